@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark of the DSA sparse-attention decode path on GB300.
+
+Workload: batched decode, B = 32 requests x 1 query row, 32768 cached tokens
+each, bf16 caches, 64 x 128 indexer, 32 MLA heads x 576-wide latent rows,
+top-2048, 64-token pages with seeded random block tables (synthetic data).
+
+A step is one dsa_decode call (indexer -> top-k -> sparse MLA split-K ->
+LSE merge) over the whole batch, inputs resident in HBM.  Between timed steps
+L2 is flushed by writing a 512 MB buffer (the step's own HBM stream, ~350 MB,
+is also larger than L2).  Each step is timed with CUDA events on the launching
+stream; `value` = rows of all ranks / max over ranks of the summed step time.
+
+`--impl reference` times the CPU oracle instead (the only other place that
+runs it is the `cpu_baseline` leg): same workload, same metric, each step a
+bounded sample of rows.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+# the CPU oracle's BLAS uses every visible core; fix the count before numpy loads
+_CORES = os.cpu_count() or 1
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+import numpy as np  # noqa: E402
+
+METRIC = "DSA decode query-rows/sec at 1 GB300; HBM GB/s as fraction of ~8 TB/s roofline"
+UNIT = "rows/s"
+WORKLOAD = ("decode B=32 x 1 row, L=32768, bf16 paged caches (page 64, random block tables), "
+            "indexer 64x128, MLA 32 heads x 576, top-2048")
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="product", choices=["product", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- ranks
+
+
+def dist_init(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n:
+        raise SystemExit(f"--gpus {n} but WORLD_SIZE={world}")
+    return rank, world, local
+
+
+def aggregate(rows_local: float, seconds_local: float, group=None, device=None):
+    """Whole-job throughput: the rows of all ranks over the slowest rank's
+    time.  Returns (value, max_seconds, total_rows)."""
+    import torch
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        t = torch.tensor([seconds_local], dtype=torch.float64, device=device)
+        n = torch.tensor([rows_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+        dist.all_reduce(n, op=dist.ReduceOp.SUM, group=group)
+        sec, rows = float(t.item()), float(n.item())
+    else:
+        sec, rows = seconds_local, rows_local
+    return rows / sec, sec, rows
+
+
+# ----------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "_build", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            ident = str(self.gpu)
+            try:
+                import torch
+                u = str(torch.cuda.get_device_properties(self.gpu).uuid)
+                ident = u if u.startswith("GPU-") else "GPU-" + u
+            except Exception:
+                pass
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        try:
+            lines = [l.strip() for l in open(self.path) if l.strip()]
+        except Exception:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in lines:
+            p = [x.strip() for x in l.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- helpers
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def kernel_source_hash(names):
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dsa_sparse_attention_decode_gb300", "csrc")
+    for n in names:
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            d = json.load(f)[kernel]
+    except Exception:
+        return None
+    if d.get("source_hash") != kernel_source_hash(d.get("sources", [])):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def algorithmic_bytes(wl):
+    """Bytes the method must move per step (what the design doc tabulates):
+    indexer key stream + block table + queries/weights; MLA selected rows +
+    indices + query + output/LSE."""
+    R, H = wl.R, wl.H
+    k = wl.topk
+    esz_k = 2 if wl.spec.dtype == "bf16" else 1
+    per_tok_idx = 128 * esz_k + (0 if esz_k == 2 else 4)
+    per_tok_kv = 576 * esz_k + (0 if esz_k == 2 else 4)
+    idx = 0
+    for b in range(wl.B):
+        L = int(wl.row_pos[wl.row_start[b + 1] - 1]) + 1
+        idx += L * per_tok_idx + ((L + 63) // 64) * 4
+    idx += R * (64 * 128 * 2 + 64 * 4)
+    mla = 0
+    for r in range(R):
+        n = min(k, int(wl.row_pos[r]) + 1)
+        mla += n * per_tok_kv + k * 4 + H * 576 * 2 + H * 512 * 4 + H * 4
+    return idx, mla
+
+
+# ----------------------------------------------------------------- product arm
+
+
+def run_product(args):
+    import torch
+
+    rank, world, local = dist_init(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    import dsa_sparse_attention_decode_gb300 as pkg
+    from dsa_sparse_attention_decode_gb300 import api
+    from workloads import config_spec, make_workload
+    from workloads.device import decode_args, upload
+
+    pkg.build()
+    pkg.lib()
+    spec = config_spec(1)
+    wl = make_workload(spec)
+    dw = upload(wl, dev)
+    R, H, k = wl.R, wl.H, wl.topk
+    out = torch.empty(R, H, 512, device=dev)
+    lse = torch.empty(R, H, device=dev)
+    tidx = torch.empty(R, k, dtype=torch.int32, device=dev)
+    tcnt = torch.empty(R, dtype=torch.int32, device=dev)
+    desc = decode_args(dw, False, out, lse, tidx, tcnt)
+    lay = api.dsa_decode_workspace_layout(desc)
+    ws = torch.zeros(lay.total_bytes, dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        api.dsa_decode(desc, ws, err, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if api.dsa_read_error(err) != 0:
+        raise SystemExit("device error word set during warm-up")
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms = timed(step, args.steps)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_sec = sum(ms) / 1e3
+    value, max_sec, total_rows = aggregate(R * args.steps, step_sec, device=dev)
+    ms_per_step = max_sec * 1e3 / args.steps
+
+    # ---- per-kernel timing of the same path (live, CUDA events, same stream)
+    scores = ws[lay.scores: lay.scores + R * lay.ld_scores * 4].view(torch.float32).view(R, lay.ld_scores)
+    valid = (dw.rows.row_pos + 1).to(torch.int32)
+    kern = {}
+    kern["indexer"] = timed(lambda: api.dsa_indexer_scores(dw.q_idx, dw.w_idx, dw.idx_k, dw.rows,
+                                                          scores, err, stream=stream), args.steps)
+    kern["topk"] = timed(lambda: api.dsa_topk(scores, valid, k, tidx, tcnt, err, stream=stream),
+                         args.steps)
+    mla_ws = torch.empty(max(1, api.dsa_sparse_mla_decode_workspace_size(R, H, k, lay.num_splits)),
+                         dtype=torch.uint8, device=dev)
+    kern["sparse_mla+lse_merge"] = timed(
+        lambda: api.dsa_sparse_mla_decode(dw.q, wl.sm_scale, dw.kv, dw.rows, tidx, tcnt, out, lse,
+                                          err, workspace=mla_ws, num_splits=lay.num_splits,
+                                          stream=stream), args.steps)
+    torch.cuda.synchronize()
+    if api.dsa_read_error(err) != 0:
+        raise SystemExit("device error word set")
+    kern_us = {n: 1e3 * float(np.mean(v)) for n, v in kern.items()}
+
+    # ---- end to end through the C ABI with host buffers
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())  # noqa: E731
+    h_in = {"q_idx": pin(dw.q_idx), "w_idx": pin(dw.w_idx), "q": pin(dw.q),
+            "row_start": pin(dw.rows.row_start), "row_pos": pin(dw.rows.row_pos),
+            "bt_idx": pin(dw.idx_k.block_table), "bt_kv": pin(dw.kv.block_table)}
+    d_in = {"q_idx": dw.q_idx, "w_idx": dw.w_idx, "q": dw.q, "row_start": dw.rows.row_start,
+            "row_pos": dw.rows.row_pos, "bt_idx": dw.idx_k.block_table,
+            "bt_kv": dw.kv.block_table}
+    h_out = pin(out)
+    h_lse = pin(lse)
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+
+    def e2e_step():
+        for n, t in h_in.items():
+            d_in[n].copy_(t, non_blocking=True)
+        api.dsa_decode(desc, ws, err, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_ms = timed(e2e_step, args.steps)
+    e2e_value, _, _ = aggregate(R * args.steps, sum(e2e_ms) / 1e3, device=dev)
+
+    # ---- roofline of the dominant kernel (the indexer: most of the bytes)
+    idx_bytes, mla_bytes = algorithmic_bytes(wl)
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    ach = idx_bytes / (kern_us["indexer"] * 1e-6) / 1e9
+    path_gbs = (idx_bytes + mla_bytes) / (ms_per_step * 1e-3) / 1e9
+    roofline = {"kernel": "indexer_kernel (dsa_indexer_scores)", "bound": "hbm",
+                "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "peak_source": peak_kind,
+                "algorithmic_bytes_per_launch": idx_bytes,
+                "traffic": ncu_traffic("indexer"),
+                "path_algorithmic_bytes_per_step": idx_bytes + mla_bytes,
+                "path_achieved_gbs": round(path_gbs, 1),
+                "path_frac_of_measured": round(path_gbs / hbm, 4),
+                "path_frac_of_nominal_8tbs": round(path_gbs / NOMINAL_HBM_GBS, 4)}
+
+    # ---- CPU oracle baseline on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    if rank == 0:
+        launches_per_step = 3 + (1 if lay.num_parts > 1 else 0)
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1)/N(0,0.5) bf16 caches and queries, U(0,1)/8 weights)",
+            "config": {"workload": WORKLOAD, "global_batch": R * world, "seq_len": 32768,
+                       "topk": k, "mla_heads": H, "num_splits": lay.num_splits,
+                       "l2": "flushed between timed steps (512 MB write); step stream ~350 MB > L2",
+                       "parallelism": f"dp{world} (independent request batches per GPU)"},
+            "roofline": roofline,
+            "kernels_us": {n: round(v, 2) for n, v in kern_us.items()},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h,
+                    "note": "per-step inputs (queries, weights, rows, block tables) from pinned "
+                            "host memory and O/LSE back; caches stay resident in HBM"},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+
+def cpu_baseline(wl, seconds: float):
+    from oracle import dsa_oracle as orc
+
+    rows, t0 = 0, time.perf_counter()
+    r = 0
+    while True:
+        orc.decode_row(wl, r % wl.R)
+        rows += 1
+        r += 1
+        el = time.perf_counter() - t0
+        if el >= seconds and rows >= 2:
+            break
+    return {"value": round(rows / el, 3), "unit": UNIT, "cores": _CORES, "kind": "oracle",
+            "sample": f"{rows} query rows of the same workload, one after another, full path "
+                      f"(indexer over 32768 tokens, exact top-2048, MLA) in float64 numpy, "
+                      f"{el:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import dsa_oracle as orc
+    from workloads import config_spec, make_workload
+
+    wl = make_workload(config_spec(1))
+    for i in range(args.warmup):
+        orc.decode_row(wl, i % wl.R)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        orc.decode_row(wl, i % wl.R)  # each step: one sampled row of the batch
+    el = time.perf_counter() - t0
+    value = args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 32, "seq_len": 32768,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": _CORES,
+                         "kind": "oracle",
+                         "sample": "one query row of the batch per step (full path, float64)"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.warmup < 3 and a.impl == "product":
+        a.warmup = 3
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_product(a)

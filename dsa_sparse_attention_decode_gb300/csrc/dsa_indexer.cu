@@ -1,0 +1,652 @@
+// DSA indexer scoring on the sm_103a tensor cores.
+//
+// "[ROCm] Support decode context parallel (DCP) for GLM-5 / DeepSeek-V3.2",
+// Motivation and Modifications / Indexer decode: every cached token (of a
+// shard) gets an indexer score before the top-2048 selection.  Score of token
+// t for query row r: sum_h w[r][h] * relu(q[r][h] . k[t]) over 64 heads x 128.
+//
+// Design (one persistent CTA per SM, 8 warps):
+//   warp 0      TMA producer: 128-token tiles of the paged index-K cache,
+//               two 64-token page halves per tile, into a ring of stages.
+//   warp 1      tcgen05 issuer: D[128 tokens x 64*rows] = K_tile . Q^T with
+//               the accumulator in TMEM (two slots, so the epilogue of one
+//               tile overlaps the MMA of the next).
+//   warps 2-3   Q staging (bf16 as is; for fp8 keys the query is turned into
+//               f16 with a per-head power-of-two scale) and, for fp8 keys, the
+//               e4m3 -> f16 conversion of each tile into the operand buffer.
+//   warps 4-7   epilogue: one thread per token row of the tile reads its
+//               TMEM lane, applies relu, the head weights (and the fp8
+//               per-token scale) and stores the fp32 score.
+// Work units are (shard, request, tile); the flattened unit list is split
+// evenly over the CTAs.  All rows of a request share one key stream.
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kTileT = 128;
+constexpr int kThreads = 256;
+constexpr int kOpBytes = kTileT * kIdxDim * 2;     // 32 KB f16/bf16 operand tile
+constexpr int kRawFp8Bytes = kTileT * kIdxDim;     // 16 KB e4m3 tile
+constexpr int kHalfBf16Box = 64 * 64 * 2;          // one TMA box: 64 tokens x 64 dims
+constexpr int kSmemLimit = 227 * 1024;
+
+struct PairMeta {           // per (shard, request) pair, written by the aux warps
+  float w[kMaxRowsPerReq][kIdxHeads];
+  int valid[kMaxRowsPerReq];
+  int row[kMaxRowsPerReq];
+};
+
+struct Layout {
+  int stages;      // TMA ring depth
+  int op_bufs;     // fp8 operand buffers
+  int stage_bytes;
+  int q_rows;      // max_rows * 64
+  int q_kb_stride; // bytes between the two 64-dim halves of Q
+  int off_ring, off_op, off_q, off_meta, off_bar, total;
+  int slot_cols, tmem_cols, rows_per_chunk;
+};
+
+__host__ __device__ inline int rows_per_chunk_of(int nr) {
+  int nch = (nr + 3) / 4;
+  return (nr + nch - 1) / nch;
+}
+
+__host__ inline Layout make_layout(int fp8, int max_rows) {
+  Layout L{};
+  L.q_rows = max_rows * kIdxHeads;
+  L.q_kb_stride = L.q_rows * 128;
+  L.rows_per_chunk = rows_per_chunk_of(max_rows);
+  L.slot_cols = L.rows_per_chunk * kIdxHeads;
+  int cols = 32;
+  while (cols < 2 * L.slot_cols) cols *= 2;
+  L.tmem_cols = cols;
+  const int q_bytes = 2 * L.q_kb_stride;
+  const int meta_bytes = 2 * static_cast<int>(sizeof(PairMeta));
+  const int bar_bytes = 512;
+  const int fixed = 1024 /*align*/ + q_bytes + meta_bytes + bar_bytes;
+  if (!fp8) {
+    L.stage_bytes = kOpBytes;
+    L.op_bufs = 0;
+    L.stages = (kSmemLimit - fixed) / kOpBytes;
+    if (L.stages > 8) L.stages = 8;
+  } else {
+    L.stage_bytes = kRawFp8Bytes;
+    L.op_bufs = 2;
+    L.stages = (kSmemLimit - fixed - 2 * kOpBytes) / kRawFp8Bytes;
+    if (L.stages > 8) L.stages = 8;
+  }
+  int off = 0;
+  L.off_ring = off;
+  off += L.stages * L.stage_bytes;
+  L.off_op = off;
+  off += L.op_bufs * kOpBytes;
+  L.off_q = off;
+  off += q_bytes;
+  L.off_meta = off;
+  off += meta_bytes;
+  L.off_bar = off;
+  off += bar_bytes;
+  L.total = off + 1024;
+  return L;
+}
+
+struct PairInfo {
+  int row0, nr, len, ntiles;
+};
+
+__device__ PairInfo pair_info(const IndexerLaunch& P, int pair, bool report) {
+  const int sl = pair / P.num_reqs;
+  const int b = pair - sl * P.num_reqs;
+  const int shard = P.shard_base + sl;
+  PairInfo pi{0, 0, 0, 0};
+  const int r0 = __ldg(P.row_start + b);
+  const int r1 = __ldg(P.row_start + b + 1);
+  if (r0 < 0 || r1 < r0 || r1 > P.num_rows) {
+    if (report) raise_err(P.d_err, DSA_DEVERR_ROWS);
+    return pi;
+  }
+  if (r1 - r0 > P.max_rows) {
+    if (report) raise_err(P.d_err, DSA_DEVERR_GROUP);
+    return pi;
+  }
+  int len = 0;
+  for (int r = r0; r < r1; ++r) {
+    const int pos = __ldg(P.row_pos + r);
+    if (pos < 0) {
+      if (report) raise_err(P.d_err, DSA_DEVERR_POS);
+      return pi;
+    }
+    len = max(len, shard_valid_len(pos, P.W, shard));
+  }
+  if (static_cast<long long>(len) >
+      static_cast<long long>(P.max_blocks[sl]) * P.page_size) {
+    if (report) raise_err(P.d_err, DSA_DEVERR_POS);
+    return pi;
+  }
+  pi.row0 = r0;
+  pi.nr = r1 - r0;
+  pi.len = len;
+  pi.ntiles = (len + kTileT - 1) / kTileT;
+  return pi;
+}
+
+// Walks this CTA's units in order: (pair, tile).
+struct Walker {
+  int pair, tile, npairs;
+  PairInfo pi;
+  __device__ void start(const IndexerLaunch& P, int p, int t) {
+    pair = p;
+    tile = t;
+    npairs = P.nshards * P.num_reqs;
+    pi = pair_info(P, pair, false);
+    skip(P);
+  }
+  __device__ void skip(const IndexerLaunch& P) {
+    while (tile >= pi.ntiles && pair + 1 < npairs) {
+      ++pair;
+      tile = 0;
+      pi = pair_info(P, pair, false);
+    }
+  }
+  __device__ void next(const IndexerLaunch& P) {
+    ++tile;
+    skip(P);
+  }
+};
+
+__device__ __forceinline__ int page_of(const IndexerLaunch& P, int sl, int b, int lp) {
+  const int32_t* bt = P.block_table[sl];
+  return bt ? __ldg(bt + static_cast<long long>(b) * P.max_blocks[sl] + lp)
+            : b * P.max_blocks[sl] + lp;
+}
+
+// e4m3 x 8 -> f16 x 8 (exact: every e4m3 value is an f16 value)
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 v) {
+  uint4 o;
+  __half2_raw h;
+  h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.x & 0xFFFFu), __NV_E4M3);
+  o.x = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+  h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.x >> 16), __NV_E4M3);
+  o.y = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+  h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.y & 0xFFFFu), __NV_E4M3);
+  o.z = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+  h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.y >> 16), __NV_E4M3);
+  o.w = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+  return o;
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kernel(const __grid_constant__ IndexerLaunch P, const Layout L) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw_base);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + L.off_bar);
+  // barrier indices
+  const int B_KFULL = 0, B_KEMPTY = 8, B_OPFULL = 16, B_OPEMPTY = 18, B_QFULL = 20,
+            B_QEMPTY = 21, B_ACCFULL = 22, B_ACCEMPTY = 24, B_PFULL = 26, B_PEMPTY = 28,
+            B_DRAIN = 30;
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 32);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 33);
+  int* s_start = reinterpret_cast<int*>(bars + 34);   // [pair, tile, nunits]
+  int* s_scan = reinterpret_cast<int*>(bars + 36);    // 8 warp sums
+  PairMeta* meta = reinterpret_cast<PairMeta*>(sbase + L.off_meta);
+
+  if (tid == 0) {
+    for (int s = 0; s < L.stages; ++s) {
+      mbar_init(bar(B_KFULL + s), 1);
+      mbar_init(bar(B_KEMPTY + s), 1);
+    }
+    for (int o = 0; o < 2; ++o) {
+      mbar_init(bar(B_OPFULL + o), 1);
+      mbar_init(bar(B_OPEMPTY + o), 1);
+      mbar_init(bar(B_ACCFULL + o), 1);
+      mbar_init(bar(B_ACCEMPTY + o), 128);
+      mbar_init(bar(B_PFULL + o), 1);
+      mbar_init(bar(B_PEMPTY + o), 128);
+    }
+    mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_QEMPTY), 1);
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < P.nshards; ++i) tma_prefetch_desc(&P.kmap[i]);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(L.tmem_cols));
+    tmem_relinquish();
+  }
+
+  // ---- schedule: count units of every (shard, request) pair, split evenly
+  const int npairs = P.nshards * P.num_reqs;
+  {
+    const int chunk = (npairs + kThreads - 1) / kThreads;
+    const int p0 = min(npairs, tid * chunk);
+    const int p1 = min(npairs, p0 + chunk);
+    int mine = 0;
+    for (int p = p0; p < p1; ++p) mine += pair_info(P, p, blockIdx.x == 0).ntiles;
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_scan[warp] = incl;
+    __syncthreads();
+    int woff = 0, total = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      if (w < warp) woff += s_scan[w];
+      total += s_scan[w];
+    }
+    const int excl = woff + incl - mine;
+    const long long u0 = static_cast<long long>(blockIdx.x) * total / gridDim.x;
+    const long long u1 = static_cast<long long>(blockIdx.x + 1) * total / gridDim.x;
+    if (tid == 0) s_start[2] = static_cast<int>(u1 - u0);
+    if (u0 < u1 && excl <= u0 && u0 < excl + mine) {
+      int acc = excl;
+      for (int p = p0; p < p1; ++p) {
+        const int n = pair_info(P, p, false).ntiles;
+        if (u0 < acc + n) {
+          s_start[0] = p;
+          s_start[1] = static_cast<int>(u0 - acc);
+          break;
+        }
+        acc += n;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int nunits = s_start[2];
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (nunits > 0) {
+    const int start_pair = s_start[0];
+    const int start_tile = s_start[1];
+    const uint32_t ring = base + L.off_ring;
+    const uint32_t opbase = base + L.off_op;
+    const uint32_t qbase = base + L.off_q;
+
+    if (warp == 0) {
+      // ------------------------------------------------ TMA producer
+      if (lane == 0) {
+        Walker wk;
+        wk.start(P, start_pair, start_tile);
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        for (int u = 0; u < nunits; ++u) {
+          if (!mbar_wait(bar(B_KEMPTY + stage), phase ^ 1u, abort_flag)) break;
+          ++issued;
+          const int sl = wk.pair / P.num_reqs;
+          const int b = wk.pair - sl * P.num_reqs;
+          int pages[2] = {-1, -1}, slots[2] = {0, 0};
+          uint32_t bytes = 0;
+          for (int h = 0; h < 2; ++h) {
+            const int t0 = wk.tile * kTileT + h * 64;
+            if (t0 >= wk.pi.len) break;
+            const int pg = page_of(P, sl, b, t0 / P.page_size);
+            if (pg < 0 || pg >= P.num_pages[sl]) {
+              raise_err(P.d_err, DSA_DEVERR_PAGE);
+              continue;
+            }
+            pages[h] = pg;
+            slots[h] = t0 % P.page_size;
+            bytes += kFp8 ? 64u * 128u : 2u * kHalfBf16Box;
+          }
+          const uint32_t fb = bar(B_KFULL + stage);
+          mbar_arrive_expect_tx(fb, bytes);
+          const uint32_t dst = ring + stage * L.stage_bytes;
+          for (int h = 0; h < 2; ++h) {
+            if (pages[h] < 0) continue;
+            if (kFp8) {
+              tma_load_3d(dst + h * 8192, &P.kmap[sl], fb, 0, slots[h], pages[h]);
+            } else {
+              tma_load_3d(dst + h * 8192, &P.kmap[sl], fb, 0, slots[h], pages[h]);
+              tma_load_3d(dst + 16384 + h * 8192, &P.kmap[sl], fb, 64, slots[h], pages[h]);
+            }
+          }
+          if (++stage == L.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          wk.next(P);
+        }
+        // every issued load must land before the CTA exits (only pending
+        // after an abort; otherwise the consumers already waited for them)
+        if (*abort_flag) {
+          volatile int no_abort = 0;
+          for (int s = 0; s < L.stages; ++s) {
+            const int last = issued - 1 - ((issued - 1 - s) % L.stages + L.stages) % L.stages;
+            if (last < 0 || (last % L.stages) != s) continue;
+            mbar_wait(bar(B_KFULL + s), static_cast<uint32_t>(last / L.stages) & 1u, &no_abort);
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        Walker wk;
+        wk.start(P, start_pair, start_tile);
+        int stage = 0;
+        uint32_t phase = 0;
+        int op = 0;
+        uint32_t op_phase = 0;
+        uint32_t acc_iter = 0;
+        int pair_j = -1, last_pair = -1;
+        for (int u = 0; u < nunits; ++u) {
+          if (wk.pair != last_pair) {
+            if (pair_j >= 0) tc_commit(bar(B_QEMPTY));
+            ++pair_j;
+            last_pair = wk.pair;
+            if (!mbar_wait(bar(B_QFULL), static_cast<uint32_t>(pair_j) & 1u, abort_flag)) break;
+            tc_fence_after();
+          }
+          uint32_t a_base;
+          if (kFp8) {
+            if (!mbar_wait(bar(B_OPFULL + op), op_phase, abort_flag)) break;
+            a_base = opbase + op * kOpBytes;
+          } else {
+            if (!mbar_wait(bar(B_KFULL + stage), phase, abort_flag)) break;
+            a_base = ring + stage * L.stage_bytes;
+          }
+          tc_fence_after();
+          const int nr = wk.pi.nr;
+          const int rpc = L.rows_per_chunk;
+          bool ok = true;
+          for (int c0 = 0; c0 < nr; c0 += rpc) {
+            const int rows_c = min(rpc, nr - c0);
+            const int slot = static_cast<int>(acc_iter & 1u);
+            const uint32_t aph = (acc_iter >> 1) & 1u;
+            if (!mbar_wait(bar(B_ACCEMPTY + slot), aph ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem_base + static_cast<uint32_t>(slot * L.slot_cols);
+            const uint32_t idesc = idesc_f16(128, rows_c * kIdxHeads, kFp8 ? 0 : 1, kFp8 ? 0 : 1);
+            const uint32_t b_base = qbase + static_cast<uint32_t>(c0 * kIdxHeads * 128);
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = smem_desc_sw128(a_base + kb * 16384 + k * 32);
+                const uint64_t bd = smem_desc_sw128(b_base + kb * L.q_kb_stride + k * 32);
+                tc_mma_f16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              }
+            }
+            tc_commit(bar(B_ACCFULL + slot));
+            ++acc_iter;
+          }
+          if (!ok) break;
+          if (kFp8) {
+            tc_commit(bar(B_OPEMPTY + op));
+            if (++op == 2) {
+              op = 0;
+              op_phase ^= 1u;
+            }
+          } else {
+            tc_commit(bar(B_KEMPTY + stage));
+            if (++stage == L.stages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          wk.next(P);
+        }
+        // all MMAs issued by this thread must finish before TMEM is freed
+        volatile int no_abort = 0;
+        tc_commit(bar(B_DRAIN));
+        mbar_wait(bar(B_DRAIN), 0u, &no_abort);
+      }
+    } else if (warp == 2 || warp == 3) {
+      // ------------------------------------------------ Q staging / fp8 convert
+      const int at = tid - 64;  // 0..63
+      Walker wk;
+      wk.start(P, start_pair, start_tile);
+      int stage = 0;
+      uint32_t phase = 0;
+      int op = 0;
+      uint32_t op_phase = 0;
+      int pair_j = -1, last_pair = -1;
+      bool ok = true;
+      for (int u = 0; u < nunits && ok; ++u) {
+        if (wk.pair != last_pair) {
+          ++pair_j;
+          last_pair = wk.pair;
+          const int mslot = pair_j & 1;
+          if (pair_j >= 2 &&
+              !mbar_wait(bar(B_PEMPTY + mslot), static_cast<uint32_t>((pair_j >> 1) - 1) & 1u,
+                         abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (pair_j >= 1 &&
+              !mbar_wait(bar(B_QEMPTY), static_cast<uint32_t>(pair_j - 1) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int sl = wk.pair / P.num_reqs;
+          const int shard = P.shard_base + sl;
+          const int nr = wk.pi.nr;
+          const int row0 = wk.pi.row0;
+          PairMeta& m = meta[mslot];
+          // one query head-row (128 dims) per thread and step
+          for (int n = at; n < nr * kIdxHeads; n += 64) {
+            const int g = n / kIdxHeads;
+            const int h = n - g * kIdxHeads;
+            const uint4* src = reinterpret_cast<const uint4*>(
+                P.q_idx + (static_cast<long long>(row0 + g) * kIdxHeads + h) * kIdxDim);
+            uint4 v[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = __ldg(src + c);
+            float wv = __ldg(P.w_idx + static_cast<long long>(row0 + g) * kIdxHeads + h);
+            if (kFp8) {
+              // scale the head's query by 2^e so that its largest |q| lands in
+              // [2^14, 2^15): every bf16 value then converts to f16 exactly
+              // (up to values 2^29 times smaller than that maximum)
+              uint32_t mx = 0;
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const uint32_t* wds = reinterpret_cast<const uint32_t*>(&v[c]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  mx = max(mx, wds[j] & 0x7FFFu);
+                  mx = max(mx, (wds[j] >> 16) & 0x7FFFu);
+                }
+              }
+              const int ebits = static_cast<int>(mx >> 7);  // biased exponent of max
+              const int e = (ebits == 0) ? 0 : max(-100, min(100, 141 - ebits));
+              const float sc = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+              wv = wv * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const uint32_t* wds = reinterpret_cast<const uint32_t*>(&v[c]);
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float lo = __uint_as_float(wds[j] << 16) * sc;
+                  const float hi = __uint_as_float(wds[j] & 0xFFFF0000u) * sc;
+                  __half2 hh = __floats2half2_rn(lo, hi);
+                  o[j] = *reinterpret_cast<uint32_t*>(&hh);
+                }
+                v[c] = make_uint4(o[0], o[1], o[2], o[3]);
+              }
+            }
+            // store into the K-major 128B-swizzled operand layout
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int kb = c >> 3;
+              const int ch = c & 7;
+              const uint32_t off = static_cast<uint32_t>(kb * L.q_kb_stride + n * 128 +
+                                                         ((ch ^ (n & 7)) << 4));
+              *reinterpret_cast<uint4*>(sbase + L.off_q + off) = v[c];
+            }
+            m.w[g][h] = wv;
+          }
+          if (at < nr) {
+            const int r = row0 + at;
+            m.row[at] = r;
+            m.valid[at] = shard_valid_len(__ldg(P.row_pos + r), P.W, shard);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 64);
+          if (at == 0) {
+            mbar_arrive(bar(B_QFULL));
+            mbar_arrive(bar(B_PFULL + mslot));
+          }
+        }
+        if (kFp8) {
+          // convert the raw e4m3 tile into the f16 operand buffer
+          if (!mbar_wait(bar(B_KFULL + stage), phase, abort_flag) ||
+              !mbar_wait(bar(B_OPEMPTY + op), op_phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* rawp = sbase + L.off_ring + stage * L.stage_bytes;
+          uint8_t* opp = sbase + L.off_op + op * kOpBytes;
+          const int wi = at >> 5;  // 0..1
+          const int l16 = lane & 15;
+          const int kb = l16 >> 3;
+          const int ch = l16 & 7;
+#pragma unroll 4
+          for (int it = 0; it < 32; ++it) {
+            const int r = (it * 2 + wi) * 2 + (lane >> 4);
+            const uint2 v = *reinterpret_cast<const uint2*>(rawp + r * 128 + l16 * 8);
+            const uint4 o = e4m3x8_to_f16x8(v);
+            *reinterpret_cast<uint4*>(opp + kb * 16384 + r * 128 + ((ch ^ (r & 7)) << 4)) = o;
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1, 64);
+          if (at == 0) {
+            mbar_arrive(bar(B_KEMPTY + stage));
+            mbar_arrive(bar(B_OPFULL + op));
+          }
+          if (++stage == L.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++op == 2) {
+            op = 0;
+            op_phase ^= 1u;
+          }
+        }
+        wk.next(P);
+      }
+    } else {
+      // ------------------------------------------------ epilogue (warps 4..7)
+      const int et = tid - 128;            // token row of the tile / TMEM lane
+      const int q4 = warp & 3;             // TMEM lane quarter of this warp
+      Walker wk;
+      wk.start(P, start_pair, start_tile);
+      uint32_t acc_iter = 0;
+      int pair_j = -1, last_pair = -1;
+      for (int u = 0; u < nunits; ++u) {
+        if (wk.pair != last_pair) {
+          if (pair_j >= 0) mbar_arrive(bar(B_PEMPTY + (pair_j & 1)));
+          ++pair_j;
+          last_pair = wk.pair;
+          if (!mbar_wait(bar(B_PFULL + (pair_j & 1)), static_cast<uint32_t>(pair_j >> 1) & 1u,
+                         abort_flag))
+            break;
+        }
+        const PairMeta& m = meta[pair_j & 1];
+        const int sl = wk.pair / P.num_reqs;
+        const int b = wk.pair - sl * P.num_reqs;
+        const int t = wk.tile * kTileT + et;
+        float kscale = 1.0f;
+        if (kFp8 && t < wk.pi.len) {
+          const int pg = page_of(P, sl, b, t / P.page_size);
+          if (pg >= 0 && pg < P.num_pages[sl])
+            kscale = __ldg(P.kscale[sl] + static_cast<long long>(pg) * P.page_size +
+                           (t % P.page_size));
+        }
+        float* out_base = P.scores + static_cast<long long>(sl) * P.shard_stride;
+        const int nr = wk.pi.nr;
+        const int rpc = L.rows_per_chunk;
+        bool ok = true;
+        for (int c0 = 0; c0 < nr; c0 += rpc) {
+          const int rows_c = min(rpc, nr - c0);
+          const int slot = static_cast<int>(acc_iter & 1u);
+          const uint32_t aph = (acc_iter >> 1) & 1u;
+          if (!mbar_wait(bar(B_ACCFULL + slot), aph, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int gi = 0; gi < rows_c; ++gi) {
+            const int g = c0 + gi;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) +
+                                   static_cast<uint32_t>(slot * L.slot_cols + gi * kIdxHeads);
+            uint32_t v0[32], v1[32];
+            tmem_ld_32x32b_x32(taddr, v0);
+            tmem_ld_32x32b_x32(taddr + 32, v1);
+            tmem_wait_ld();
+            float s = 0.0f;
+#pragma unroll
+            for (int h = 0; h < 32; ++h) s = fmaf(m.w[g][h], fmaxf(__uint_as_float(v0[h]), 0.0f), s);
+#pragma unroll
+            for (int h = 0; h < 32; ++h)
+              s = fmaf(m.w[g][32 + h], fmaxf(__uint_as_float(v1[h]), 0.0f), s);
+            if (t < m.valid[g]) {
+              out_base[static_cast<long long>(m.row[g]) * P.ld + t] = s * kscale;
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(bar(B_ACCEMPTY + slot));
+          ++acc_iter;
+        }
+        if (!ok) break;
+        wk.next(P);
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) raise_err(P.d_err, DSA_DEVERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, static_cast<uint32_t>(L.tmem_cols));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_indexer(const IndexerLaunch& p, cudaStream_t stream) {
+  const Layout L = make_layout(p.fp8, p.max_rows);
+  if (L.stages < 2) return cudaErrorInvalidValue;
+  int grid = num_sms();
+  if (grid <= 0) return cudaErrorInvalidDevice;
+  cudaError_t e;
+  if (p.fp8) {
+    e = cudaFuncSetAttribute(indexer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L.total);
+    if (e != cudaSuccess) return e;
+    indexer_kernel<true><<<grid, kThreads, L.total, stream>>>(p, L);
+  } else {
+    e = cudaFuncSetAttribute(indexer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L.total);
+    if (e != cudaSuccess) return e;
+    indexer_kernel<false><<<grid, kThreads, L.total, stream>>>(p, L);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

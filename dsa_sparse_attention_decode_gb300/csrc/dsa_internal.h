@@ -1,0 +1,122 @@
+// Launchers of the kernels behind the C ABI (host side).  Every launcher only
+// enqueues work on `stream`; argument validation happens in dsa_abi.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dsa_decode.h"
+
+namespace dsa {
+
+// ------------------------------------------------------------- indexer
+
+// One launch scores the rows against `num_shards_in_launch` shard caches
+// (shard ids shard_base .. shard_base + n - 1 of a group of W shards).
+struct IndexerLaunch {
+  CUtensorMap kmap[DSA_MAX_SHARDS];       // index-K tensor maps (TMA)
+  const int32_t* block_table[DSA_MAX_SHARDS];
+  const float* kscale[DSA_MAX_SHARDS];    // fp8 per-token scales
+  int32_t num_pages[DSA_MAX_SHARDS];
+  int32_t max_blocks[DSA_MAX_SHARDS];
+  int32_t page_size;
+  int32_t fp8;
+  int32_t W;            // shards of the group
+  int32_t shard_base;   // id of kmap[0]
+  int32_t nshards;      // caches in this launch
+  const uint16_t* q_idx;
+  const float* w_idx;
+  const int32_t* row_start;
+  const int32_t* row_pos;
+  int32_t num_rows;
+  int32_t num_reqs;
+  int32_t max_rows;     // rows per request bound (1..8)
+  float* scores;        // cache i writes rows at scores + i * shard_stride
+  int64_t ld;
+  int64_t shard_stride;
+  int32_t* d_err;
+};
+
+// Host: fill kmap[i] for a cache; returns cudaSuccess or an error.
+cudaError_t make_index_k_tmap(CUtensorMap* map, const dsa_paged_cache& c);
+cudaError_t launch_indexer(const IndexerLaunch& p, cudaStream_t stream);
+
+// ------------------------------------------------------------- top-k
+
+struct TopkLaunch {
+  const float* scores;
+  int64_t ld;
+  int64_t shard_stride;       // scores of row q = w * R + r at scores + w*stride + r*ld
+  const int32_t* valid_len;   // explicit per-row valid counts, or NULL:
+  const int32_t* row_pos;     //   valid = shard_valid_len(row_pos[r], W, w)
+  int32_t W;
+  int32_t shard_offset;       // shard id of w = 0 (single-shard calls)
+  int32_t rows;               // R (rows per shard)
+  int32_t nshards;            // shards in this launch (grid = nshards * R)
+  int32_t k;
+  int32_t index_stride;       // out index = j * stride + (w + shard_offset) * per_shard_offset
+  int32_t index_offset;
+  int32_t offset_per_shard;   // 1: add the shard id to index_offset
+  int32_t* out_idx;           // row q at out_idx + q * k
+  float* out_score;           // or NULL
+  int32_t* out_count;
+  int32_t* d_err;
+};
+cudaError_t launch_topk(const TopkLaunch& p, cudaStream_t stream);
+
+// ------------------------------------------------------------- shard merge
+
+struct MergeTopkLaunch {
+  const float* cand_score;
+  const int32_t* cand_pos;
+  const int32_t* cand_count;
+  int32_t W, rows, k;
+  int32_t* out_idx;
+  int32_t* out_count;
+  int32_t* owned_local;
+  int32_t* owned_count;
+  int32_t* d_err;
+};
+cudaError_t launch_shard_topk_merge(const MergeTopkLaunch& p, cudaStream_t stream);
+
+// ------------------------------------------------------------- sparse MLA
+
+struct MlaLaunch {
+  const void* kv[DSA_MAX_SHARDS];
+  const float* kscale[DSA_MAX_SHARDS];
+  const int32_t* block_table[DSA_MAX_SHARDS];
+  int32_t num_pages[DSA_MAX_SHARDS];
+  int32_t max_blocks[DSA_MAX_SHARDS];
+  int32_t page_size;
+  int32_t fp8;
+  int32_t nshards;         // caches in this launch; work row q = w * R + r
+  const uint16_t* q;       // [R][H][576]
+  int32_t heads;
+  float sm_scale;
+  const int32_t* row_start;
+  int32_t num_reqs;
+  int32_t rows;            // R
+  const int32_t* idx;      // row q's list at idx + q * k
+  const int32_t* count;    // [nshards * R]
+  int32_t k;
+  int32_t num_splits;      // S
+  int32_t chunk;           // tokens per split (multiple of 64)
+  float* out;              // when parts == 1: [R][H][512]
+  float* out_lse;
+  float* part_out;         // else: part p = w * S + s at part_out + p*R*H*512
+  float* part_lse;
+  int32_t* d_err;
+};
+cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream);
+int auto_mla_splits(int work_rows, int k, int expected_count);
+
+// ------------------------------------------------------------- LSE merge
+
+cudaError_t launch_lse_merge(const float* O_parts, const float* lse_parts, int parts,
+                             int rows, int heads, int dv, float* out, float* out_lse,
+                             cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace dsa

@@ -1,0 +1,529 @@
+// Absorbed-MLA sparse decode, split-K with LSE.
+//
+// "[ROCm] Support decode context parallel (DCP) for GLM-5 / DeepSeek-V3.2",
+// Modifications / Sparse decode: every (shard of a) query row attends only
+// its selected latent rows with a split-K kernel that also returns the
+// natural-log LSE; the commit "store a lone split's output and LSE in place":
+// with a single split the partial is the final result and goes straight to
+// the caller's output.
+//
+// One CTA (8 warps) per (work row, split).  The split's selected positions are
+// resolved through the block table once; then 64-token tiles of 576-wide
+// latent rows are gathered with 16-byte cp.async into a double buffer (fp8
+// rows are widened to f16 in shared memory: e4m3 values are f16 values) and
+// every head of the row shares each gathered tile:
+//   S = q . kv^T (all 576 dims), online softmax in fp32 (base 2), P rounded to
+//   the MMA input type, O += P . v (first 512 dims).
+// The fp8 path multiplies each logit by the token's scale and folds the scale
+// into P for the value product; its query is converted to f16 with a per-head
+// power-of-two factor that the logit scale undoes.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTile = 64;                 // tokens per tile
+constexpr int kRowB = kKvDim * 2 + 16;    // padded smem row of 576 16-bit values
+constexpr int kPRowB = kTile * 2 + 16;    // padded smem row of P
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct MlaSmem {
+  int off_q, off_kv, off_raw, off_p, off_red, off_rowoff, off_kscale, off_misc, total;
+  int kv_bufs;
+};
+
+__host__ __device__ inline MlaSmem mla_smem(int heads, int fp8, int chunk) {
+  MlaSmem s{};
+  int off = 0;
+  s.off_q = off;
+  off += heads * kRowB;
+  s.kv_bufs = fp8 ? 1 : 2;
+  s.off_kv = off;
+  off += s.kv_bufs * kTile * kRowB;
+  s.off_raw = off;
+  off += fp8 ? 2 * kTile * kKvDim : 0;
+  s.off_p = off;
+  off += heads * kPRowB;
+  s.off_red = off;
+  off += 2 * 8 * heads * 4;
+  s.off_rowoff = off;
+  off += chunk * 8;
+  s.off_kscale = off;
+  off += fp8 ? chunk * 4 : 0;
+  s.off_misc = off;
+  off += 64 * 4 + heads * 4;
+  s.total = off;
+  return s;
+}
+
+DSA_DEV void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+DSA_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+DSA_DEV void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+DSA_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+DSA_DEV void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+DSA_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+template <bool kF16>
+DSA_DEV void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                      uint32_t b1) {
+  if (kF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+template <bool kF16>
+DSA_DEV uint32_t pack2(float lo, float hi) {
+  if (kF16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+// H heads (16 or 32); kFp8: e4m3 cache, f16 MMAs; else bf16 cache and MMAs.
+template <int H, bool kFp8>
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch P) {
+  constexpr int MT = H / 16;             // m16 tiles of heads
+  constexpr int NTW = MT;                // n8 token tiles per warp in S = q.kv^T
+  constexpr int TGS = 8 / MT;            // token groups
+  extern __shared__ __align__(16) uint8_t smem[];
+  const MlaSmem S = mla_smem(H, kFp8, P.chunk);
+  uint8_t* q_s = smem + S.off_q;
+  uint8_t* kv_s = smem + S.off_kv;
+  uint8_t* raw_s = smem + S.off_raw;
+  uint8_t* p_s = smem + S.off_p;
+  float* red = reinterpret_cast<float*>(smem + S.off_red);      // [2][TGS][H]
+  long long* rowoff = reinterpret_cast<long long*>(smem + S.off_rowoff);
+  float* kscale_s = reinterpret_cast<float*>(smem + S.off_kscale);
+  int* misc = reinterpret_cast<int*>(smem + S.off_misc);
+  float* qexp = reinterpret_cast<float*>(smem + S.off_misc + 64 * 4);  // [H] logit scales
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int split = blockIdx.x;
+  const int qrow = blockIdx.y;                 // w * R + r
+  const int w = qrow / P.rows;
+  const int r = qrow - w * P.rows;
+  const int part = w * P.num_splits + split;
+  const bool direct = (P.nshards * P.num_splits == 1);
+
+  int cnt = __ldg(P.count + qrow);
+  if (cnt < 0 || cnt > P.k) {
+    if (tid == 0) raise_err(P.d_err, DSA_DEVERR_INDEX);
+    cnt = cnt < 0 ? 0 : P.k;
+  }
+  const int begin = split * P.chunk;
+  const int ntok = max(0, min(cnt, begin + P.chunk) - begin);
+
+  float* out_o = direct ? P.out + static_cast<long long>(r) * H * kVDim
+                        : P.part_out + (static_cast<long long>(part) * P.rows + r) * H * kVDim;
+  float* out_l = direct ? P.out_lse + static_cast<long long>(r) * H
+                        : P.part_lse + (static_cast<long long>(part) * P.rows + r) * H;
+  if (ntok == 0) {
+    for (int h = tid; h < H; h += kThreads) out_l[h] = -__int_as_float(0x7f800000);
+    if (direct)
+      for (int i = tid; i < H * kVDim; i += kThreads) out_o[i] = 0.0f;
+    return;
+  }
+
+  // request of this row
+  if (tid == 0) {
+    int lo = 0, hi = P.num_reqs - 1, b = -1;
+    while (lo <= hi) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(P.row_start + mid) <= r) {
+        b = mid;
+        lo = mid + 1;
+      } else {
+        hi = mid - 1;
+      }
+    }
+    if (b < 0 || r >= __ldg(P.row_start + b + 1)) {
+      raise_err(P.d_err, DSA_DEVERR_ROWS);
+      b = -1;
+    }
+    misc[0] = b;
+  }
+
+  // query -> smem (bf16 copy; fp8 path: f16 with a per-head power of two)
+  const uint16_t* qsrc = P.q + static_cast<long long>(r) * H * kKvDim;
+  if (!kFp8) {
+    for (int c = tid; c < H * 72; c += kThreads) {
+      const int h = c / 72, cc = c - h * 72;
+      cp_async16(smem_u32(q_s + h * kRowB + cc * 16), qsrc + h * kKvDim + cc * 8);
+    }
+    cp_async_commit();
+    if (tid < H) qexp[tid] = P.sm_scale * kLog2e;
+  } else {
+    // one warp per head: max |q| -> exponent -> scaled f16 copy
+    for (int h = warp; h < H; h += 8) {
+      const uint16_t* src = qsrc + h * kKvDim;
+      uint32_t mx = 0;
+      for (int i = lane; i < kKvDim; i += 32) mx = max(mx, static_cast<uint32_t>(src[i] & 0x7FFFu));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const int ebits = static_cast<int>(mx >> 7);
+      const int e = (ebits == 0) ? 0 : max(-100, min(100, 141 - ebits));
+      const float sc = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+      for (int i = lane; i < kKvDim / 2; i += 32) {
+        const uint32_t two = *reinterpret_cast<const uint32_t*>(src + 2 * i);
+        const float lo = __uint_as_float(two << 16) * sc;
+        const float hi = __uint_as_float(two & 0xFFFF0000u) * sc;
+        *reinterpret_cast<uint32_t*>(q_s + h * kRowB + i * 4) = pack2<true>(lo, hi);
+      }
+      if (lane == 0)
+        qexp[h] = P.sm_scale * kLog2e * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    }
+  }
+  __syncthreads();
+
+  // resolve the split's positions to element offsets
+  const int b = misc[0];
+  const int32_t* bt = P.block_table[w];
+  const int psz = P.page_size;
+  const int32_t* ilist = P.idx + static_cast<long long>(qrow) * P.k + begin;
+  for (int i = tid; i < ntok; i += kThreads) {
+    const int t = __ldg(ilist + i);
+    long long off = -1;
+    if (b >= 0 && t >= 0 && static_cast<long long>(t) < static_cast<long long>(P.max_blocks[w]) * psz) {
+      const int lp = t / psz;
+      const int pg = bt ? __ldg(bt + static_cast<long long>(b) * P.max_blocks[w] + lp)
+                        : b * P.max_blocks[w] + lp;
+      if (pg >= 0 && pg < P.num_pages[w]) {
+        off = static_cast<long long>(pg) * psz + (t - lp * psz);
+      } else {
+        raise_err(P.d_err, DSA_DEVERR_PAGE);
+      }
+    } else {
+      raise_err(P.d_err, DSA_DEVERR_INDEX);
+    }
+    rowoff[i] = off;
+    if (kFp8) kscale_s[i] = off >= 0 ? __ldg(P.kscale[w] + off) : 0.0f;
+  }
+  __syncthreads();
+
+  const uint8_t* kvbase = static_cast<const uint8_t*>(P.kv[w]);
+  const int ntiles = (ntok + kTile - 1) / kTile;
+
+  auto issue_gather = [&](int tile, int buf) {
+    const int t0 = tile * kTile;
+    if (!kFp8) {
+      uint8_t* dst = kv_s + buf * kTile * kRowB;
+      for (int c = tid; c < kTile * 72; c += kThreads) {
+        const int row = c / 72, cc = c - row * 72;
+        const long long off = (t0 + row < ntok) ? rowoff[t0 + row] : -1;
+        if (off >= 0) {
+          cp_async16(smem_u32(dst + row * kRowB + cc * 16), kvbase + off * (kKvDim * 2) + cc * 16);
+        } else {
+          *reinterpret_cast<uint4*>(dst + row * kRowB + cc * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    } else {
+      uint8_t* dst = raw_s + buf * kTile * kKvDim;
+      for (int c = tid; c < kTile * 36; c += kThreads) {
+        const int row = c / 36, cc = c - row * 36;
+        const long long off = (t0 + row < ntok) ? rowoff[t0 + row] : -1;
+        if (off >= 0) {
+          cp_async16(smem_u32(dst + row * kKvDim + cc * 16), kvbase + off * kKvDim + cc * 16);
+        } else {
+          *reinterpret_cast<uint4*>(dst + row * kKvDim + cc * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+  // per-thread state: O accumulators for dims [64*warp, 64*warp+64) of all heads
+  float o[MT][8][4];
+#pragma unroll
+  for (int a = 0; a < MT; ++a)
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) o[a][j][c] = 0.0f;
+  float m_run[MT][2];
+#pragma unroll
+  for (int a = 0; a < MT; ++a) m_run[a][0] = m_run[a][1] = -__int_as_float(0x7f800000);
+  float l_part[2] = {0.0f, 0.0f};  // row sums of this thread's S rows
+
+  const int mt_s = warp % MT;          // S role: head tile
+  const int tg = warp / MT;            // S role: token group
+  const int n_s0 = tg * (8 * NTW);     // first token of the group in the tile
+  const float qsc0 = qexp[mt_s * 16 + g];
+  const float qsc1 = qexp[mt_s * 16 + g + 8];
+
+  issue_gather(0, 0);
+  for (int tile = 0; tile < ntiles; ++tile) {
+    const int buf = kFp8 ? 0 : (tile & 1);
+    if (tile + 1 < ntiles) {
+      issue_gather(tile + 1, kFp8 ? ((tile + 1) & 1) : ((tile + 1) & 1));
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    uint8_t* kv = kv_s + buf * kTile * kRowB;
+    if (kFp8) {
+      const uint8_t* rawp = raw_s + (tile & 1) * kTile * kKvDim;
+      for (int c = tid; c < kTile * 72; c += kThreads) {
+        const int row = c / 72, cc = c - row * 72;
+        const uint2 v = *reinterpret_cast<const uint2*>(rawp + row * kKvDim + cc * 8);
+        uint4 out;
+        __half2_raw h;
+        h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.x & 0xFFFFu), __NV_E4M3);
+        out.x = h.x | (static_cast<uint32_t>(h.y) << 16);
+        h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.x >> 16), __NV_E4M3);
+        out.y = h.x | (static_cast<uint32_t>(h.y) << 16);
+        h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.y & 0xFFFFu), __NV_E4M3);
+        out.z = h.x | (static_cast<uint32_t>(h.y) << 16);
+        h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.y >> 16), __NV_E4M3);
+        out.w = h.x | (static_cast<uint32_t>(h.y) << 16);
+        *reinterpret_cast<uint4*>(kv + row * kRowB + cc * 16) = out;
+      }
+      __syncthreads();
+    }
+    const int t0 = tile * kTile;
+    const uint32_t kv_a = smem_u32(kv);
+    const uint32_t q_a = smem_u32(q_s);
+
+    // ---- S = q . kv^T for head tile mt_s, tokens n_s0 .. n_s0 + 8*NTW
+    float sacc[NTW][4];
+#pragma unroll
+    for (int j = 0; j < NTW; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.0f;
+    {
+      const uint32_t a_addr = q_a + (mt_s * 16 + (lane & 15)) * kRowB + (lane >> 4) * 16;
+#pragma unroll 4
+      for (int kk = 0; kk < kKvDim / 16; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(a_addr + kk * 32, a0, a1, a2, a3);
+        if (NTW == 2) {
+          uint32_t b0, b1, b2, b3;
+          const int trow = n_s0 + (lane & 7) + ((lane >> 4) << 3);
+          ldsm_x4(kv_a + trow * kRowB + kk * 32 + ((lane >> 3) & 1) * 16, b0, b1, b2, b3);
+          mma16816<kFp8>(sacc[0], a0, a1, a2, a3, b0, b1);
+          mma16816<kFp8>(sacc[NTW - 1], a0, a1, a2, a3, b2, b3);
+        } else {
+          uint32_t b0, b1;
+          const int trow = n_s0 + (lane & 7);
+          ldsm_x2(kv_a + trow * kRowB + kk * 32 + ((lane >> 3) & 1) * 16, b0, b1);
+          mma16816<kFp8>(sacc[0], a0, a1, a2, a3, b0, b1);
+        }
+      }
+    }
+    // logits in base 2, masked past the split's end
+    float mx0 = -__int_as_float(0x7f800000), mx1 = mx0;
+#pragma unroll
+    for (int j = 0; j < NTW; ++j) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int tok = n_s0 + 8 * j + 2 * t4 + c;
+        const bool ok = t0 + tok < ntok;
+        float ks = 1.0f;
+        if (kFp8) ks = ok ? kscale_s[t0 + tok] : 0.0f;
+        const float z0 = ok ? sacc[j][c] * qsc0 * ks : -__int_as_float(0x7f800000);
+        const float z1 = ok ? sacc[j][2 + c] * qsc1 * ks : -__int_as_float(0x7f800000);
+        sacc[j][c] = z0;
+        sacc[j][2 + c] = z1;
+        mx0 = fmaxf(mx0, z0);
+        mx1 = fmaxf(mx1, z1);
+      }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    if (t4 == 0) {
+      red[tg * H + mt_s * 16 + g] = mx0;
+      red[tg * H + mt_s * 16 + g + 8] = mx1;
+    }
+    __syncthreads();
+    // new running max for every head row this thread touches
+    float alpha[MT][2];
+#pragma unroll
+    for (int a = 0; a < MT; ++a) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = a * 16 + g + hh * 8;
+        float tm = red[h];
+#pragma unroll
+        for (int x = 1; x < TGS; ++x) tm = fmaxf(tm, red[x * H + h]);
+        const float mn = fmaxf(m_run[a][hh], tm);
+        const float msafe = (mn == -__int_as_float(0x7f800000)) ? 0.0f : mn;
+        alpha[a][hh] = exp2f(m_run[a][hh] - msafe);
+        m_run[a][hh] = mn;
+      }
+    }
+    // P for the S rows of this warp
+    {
+      const float mA = (m_run[mt_s][0] == -__int_as_float(0x7f800000)) ? 0.0f : m_run[mt_s][0];
+      const float mB = (m_run[mt_s][1] == -__int_as_float(0x7f800000)) ? 0.0f : m_run[mt_s][1];
+      float ls0 = 0.0f, ls1 = 0.0f;
+#pragma unroll
+      for (int j = 0; j < NTW; ++j) {
+        const int tok = n_s0 + 8 * j + 2 * t4;
+        const float p00 = exp2f(sacc[j][0] - mA), p01 = exp2f(sacc[j][1] - mA);
+        const float p10 = exp2f(sacc[j][2] - mB), p11 = exp2f(sacc[j][3] - mB);
+        ls0 += p00 + p01;
+        ls1 += p10 + p11;
+        float v00 = p00, v01 = p01, v10 = p10, v11 = p11;
+        if (kFp8) {
+          const float k0 = (t0 + tok < ntok) ? kscale_s[t0 + tok] : 0.0f;
+          const float k1 = (t0 + tok + 1 < ntok) ? kscale_s[t0 + tok + 1] : 0.0f;
+          v00 *= k0;
+          v01 *= k1;
+          v10 *= k0;
+          v11 *= k1;
+        }
+        *reinterpret_cast<uint32_t*>(p_s + (mt_s * 16 + g) * kPRowB + tok * 2) = pack2<kFp8>(v00, v01);
+        *reinterpret_cast<uint32_t*>(p_s + (mt_s * 16 + g + 8) * kPRowB + tok * 2) =
+            pack2<kFp8>(v10, v11);
+      }
+      l_part[0] = l_part[0] * alpha[mt_s][0] + ls0;
+      l_part[1] = l_part[1] * alpha[mt_s][1] + ls1;
+    }
+    __syncthreads();
+
+    // ---- O += P . v for value dims [64*warp, 64*warp + 64)
+#pragma unroll
+    for (int a = 0; a < MT; ++a)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        o[a][j][0] *= alpha[a][0];
+        o[a][j][1] *= alpha[a][0];
+        o[a][j][2] *= alpha[a][1];
+        o[a][j][3] *= alpha[a][1];
+      }
+    {
+      const uint32_t p_a = smem_u32(p_s);
+      const int d0 = warp * 64;
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        uint32_t af[MT][4];
+#pragma unroll
+        for (int a = 0; a < MT; ++a)
+          ldsm_x4(p_a + (a * 16 + (lane & 15)) * kPRowB + kk * 32 + (lane >> 4) * 16, af[a][0],
+                  af[a][1], af[a][2], af[a][3]);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          uint32_t b0, b1, b2, b3;
+          const int trow = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int dcol = d0 + (j + (lane >> 4)) * 8;
+          ldsm_x4_t(kv_a + trow * kRowB + dcol * 2, b0, b1, b2, b3);
+#pragma unroll
+          for (int a = 0; a < MT; ++a) {
+            mma16816<kFp8>(o[a][j], af[a][0], af[a][1], af[a][2], af[a][3], b0, b1);
+            mma16816<kFp8>(o[a][j + 1], af[a][0], af[a][1], af[a][2], af[a][3], b2, b3);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- softmax denominators: sum the row partials over t4 and token groups
+  float l0 = l_part[0], l1 = l_part[1];
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  float* red2 = red + TGS * H;
+  if (t4 == 0) {
+    red2[tg * H + mt_s * 16 + g] = l0;
+    red2[tg * H + mt_s * 16 + g + 8] = l1;
+  }
+  __syncthreads();
+  const int d0 = warp * 64;
+#pragma unroll
+  for (int a = 0; a < MT; ++a) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int h = a * 16 + g + hh * 8;
+      float l = 0.0f;
+#pragma unroll
+      for (int x = 0; x < TGS; ++x) l += red2[x * H + h];
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float2 v = make_float2(o[a][j][2 * hh] * inv, o[a][j][2 * hh + 1] * inv);
+        *reinterpret_cast<float2*>(out_o + h * kVDim + d0 + 8 * j + 2 * t4) = v;
+      }
+      if (warp == 0 && t4 == 0) {
+        out_l[h] = l > 0.0f ? (m_run[a][hh] + log2f(l)) * kLn2 : -__int_as_float(0x7f800000);
+      }
+    }
+  }
+}
+
+template <int H, bool F>
+cudaError_t launch_one(const MlaLaunch& p, cudaStream_t stream) {
+  const MlaSmem S = mla_smem(H, F, p.chunk);
+  cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel<H, F>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, S.total);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.num_splits, p.nshards * p.rows);
+  sparse_mla_kernel<H, F><<<grid, kThreads, S.total, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int mla_smem_bytes(int heads, int fp8, int chunk) { return mla_smem(heads, fp8, chunk).total; }
+
+int auto_mla_splits(int work_rows, int k, int expected_count) {
+  // aim for about one CTA per SM; splits are whole 64-token tiles
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  int target = sms / (work_rows > 0 ? work_rows : 1);
+  if (target < 1) target = 1;
+  int per = (expected_count + target - 1) / target;
+  per = ((per + kTile - 1) / kTile) * kTile;
+  if (per < kTile) per = kTile;
+  int s = (k + per - 1) / per;
+  if (s < 1) s = 1;
+  return s;
+}
+
+cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream) {
+  if (p.nshards * p.rows == 0 || p.num_splits == 0) return cudaSuccess;
+  if (p.heads == 16) return p.fp8 ? launch_one<16, true>(p, stream) : launch_one<16, false>(p, stream);
+  if (p.heads == 32) return p.fp8 ? launch_one<32, true>(p, stream) : launch_one<32, false>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dsa

@@ -1,0 +1,110 @@
+"""Parity of the fused dsa_decode path against the CPU oracle on all five
+workload configurations: reduced sizes (every row checked) and full sizes
+(sampled rows), plus sharded == unsharded."""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from oracle import dsa_oracle as orc  # noqa: E402
+from workloads import config_spec, make_workload  # noqa: E402
+from workloads.device import upload  # noqa: E402
+
+from gpu_util import DecodeRun, check_decode_rows  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(spec, sharded=False, num_splits=0, rows=None):
+    wl = make_workload(spec)
+    dw = upload(wl, "cuda")
+    run = DecodeRun(dw, sharded=sharded, num_splits=num_splits)
+    assert run.run() == 0
+    rows = range(wl.R) if rows is None else rows
+    return wl, run, check_decode_rows(run, rows)
+
+
+def test_config0_full():
+    _run(config_spec(0))
+
+
+@pytest.mark.parametrize("L", [300, 2048, 2049, 5000])
+def test_config1_reduced(L):
+    _run(config_spec(1, B=3, L=L))
+
+
+def test_config2_reduced_mtp_fp8():
+    _run(config_spec(2, B=3, L_lo=1500, L_hi=6000))
+
+
+@pytest.mark.parametrize("W,L", [(2, 5001), (3, 6007), (4, 9001)])
+def test_config3_reduced_sharded(W, L):
+    _run(config_spec(3, B=2, L=L, shards=W), sharded=True)
+
+
+def test_config4_reduced_ragged_fp8():
+    _run(config_spec(4, B=9, L_lo=300, L_hi=12000))
+
+
+@pytest.mark.parametrize("S", [1, 2, 7, 32])
+def test_split_counts_agree(S):
+    _run(config_spec(1, B=2, L=4500), num_splits=S)
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4])
+def test_sharded_equals_unsharded_bit_exact(W):
+    wl = make_workload(config_spec(3, B=2, L=7777, shards=W))
+    dw = upload(wl, "cuda")
+    a = DecodeRun(dw, sharded=False)
+    b = DecodeRun(dw, sharded=True)
+    assert a.run() == 0 and b.run() == 0
+    for r in range(wl.R):
+        full = a.scores(r)
+        for w in range(W):
+            assert np.array_equal(b.scores(r, w).view(np.uint32), full[w::W].view(np.uint32))
+    assert torch.equal(a.idx, b.idx) and torch.equal(a.cnt, b.cnt)
+    o_a, o_b = a.out.cpu().numpy(), b.out.cpu().numpy()
+    rel = np.abs(o_a - o_b).max(axis=-1) / np.abs(o_a).max(axis=-1)
+    assert rel.max() <= 2e-3
+    assert np.abs(a.lse.cpu().numpy() - b.lse.cpu().numpy()).max() <= 1e-4
+
+
+def test_deterministic():
+    wl = make_workload(config_spec(2, B=2, L_lo=3000, L_hi=5000))
+    dw = upload(wl, "cuda")
+    a = DecodeRun(dw)
+    assert a.run() == 0
+    o1, l1, i1 = a.out.clone(), a.lse.clone(), a.idx.clone()
+    assert a.run() == 0
+    assert torch.equal(o1, a.out) and torch.equal(l1, a.lse) and torch.equal(i1, a.idx)
+
+
+# ------------------------------------------------------------- full sizes
+
+
+def test_config1_full_size_sampled():
+    """The benchmark's workload (B=32, L=32768, bf16, paged), 4 rows checked."""
+    _run(config_spec(1), rows=[0, 7, 19, 31])
+
+
+def test_config2_full_size_sampled():
+    wl = make_workload(config_spec(2))
+    dw = upload(wl, "cuda")
+    run = DecodeRun(dw)
+    assert run.run() == 0
+    check_decode_rows(run, [0, 1, 5, 6 * 37 + 3, wl.R - 1])
+
+
+def test_config3_full_size():
+    _run(config_spec(3), sharded=True)
+
+
+def test_config4_full_size_sampled():
+    wl = make_workload(config_spec(4, B=64))
+    dw = upload(wl, "cuda")
+    run = DecodeRun(dw)
+    assert run.run() == 0
+    longest = int(np.argmax(wl.seq_len))
+    shortest = int(np.argmin(wl.seq_len))
+    check_decode_rows(run, sorted({0, longest, shortest, 33, 63}))

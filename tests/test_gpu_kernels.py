@@ -1,0 +1,261 @@
+"""The individual entry points through the C ABI against the CPU oracle, and
+the edge cases: ties, short rows, single tokens, device-side error checks."""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from dsa_sparse_attention_decode_gb300 import api  # noqa: E402
+from dsa_sparse_attention_decode_gb300 import _lib as C  # noqa: E402
+from oracle import dsa_oracle as orc  # noqa: E402
+from workloads import config_spec, make_workload  # noqa: E402
+from workloads.device import upload  # noqa: E402
+
+from gpu_util import DecodeRun, attn_err, check_decode_rows, score_ok  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _err():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+@pytest.mark.parametrize("cfg,kw", [(1, dict(B=3, L=1000)), (2, dict(B=2, L_lo=700, L_hi=1500)),
+                                    (0, {})])
+def test_indexer_scores(cfg, kw):
+    wl = make_workload(config_spec(cfg, **kw))
+    dw = upload(wl, DEV)
+    ld = dw.rows.max_len + 3
+    scores = torch.full((wl.R, ld), 12345.0, device=DEV)
+    err = _err()
+    api.dsa_indexer_scores(dw.q_idx, dw.w_idx, dw.idx_k, dw.rows, scores, err)
+    assert api.dsa_read_error(err) == 0
+    s = scores.cpu().numpy()
+    for r in range(wl.R):
+        n = int(wl.row_pos[r]) + 1
+        ok, e = score_ok(s[r, :n], orc.row_scores(wl, r))
+        assert ok, (r, e)
+        assert np.all(s[r, n:] == 12345.0), "wrote past the row's valid length"
+
+
+def test_indexer_single_shard_call():
+    wl = make_workload(config_spec(3, B=2, L=3001, shards=3))
+    dw = upload(wl, DEV)
+    for w in range(3):
+        n = (dw.rows.max_len + 2) // 3
+        scores = torch.zeros((wl.R, n), device=DEV)
+        err = _err()
+        api.dsa_indexer_scores(dw.q_idx, dw.w_idx, dw.idx_k_shards[w], dw.rows, scores, err,
+                               shard=w, num_shards=3)
+        assert api.dsa_read_error(err) == 0
+        for r in range(wl.R):
+            m = orc.shard_valid_len(int(wl.row_pos[r]), 3, w)
+            ok, e = score_ok(scores[r, :m].cpu().numpy(),
+                             orc.row_scores(wl, r, wl.idx_k_shards[w], 3, w))
+            assert ok, (w, r, e)
+
+
+def _topk_case(s: np.ndarray, valid: np.ndarray, k: int, stride=1, offset=0):
+    R = s.shape[0]
+    st = torch.from_numpy(s.astype(np.float32)).to(DEV)
+    vt = torch.from_numpy(valid.astype(np.int32)).to(DEV)
+    oi = torch.full((R, k), -5, dtype=torch.int32, device=DEV)
+    os_ = torch.zeros((R, k), dtype=torch.float32, device=DEV)
+    oc = torch.zeros(R, dtype=torch.int32, device=DEV)
+    err = _err()
+    api.dsa_topk(st, vt, k, oi, oc, err, out_score=os_, index_stride=stride, index_offset=offset)
+    e = api.dsa_read_error(err)
+    oi, os_, oc = oi.cpu().numpy(), os_.cpu().numpy(), oc.cpu().numpy()
+    for r in range(R):
+        n = int(valid[r])
+        want = orc.topk_select(s[r, :n].astype(np.float32).astype(np.float64), k)
+        assert oc[r] == len(want)
+        assert np.array_equal(oi[r, : oc[r]], want * stride + offset), r
+        assert np.all(oi[r, oc[r]:] == -1)
+        assert np.array_equal(os_[r, : oc[r]], s[r, want].astype(np.float32))
+    return e
+
+
+def test_topk_random_rows():
+    rng = np.random.default_rng(0)
+    R, L = 6, 70000
+    s = rng.standard_normal((R, L)).astype(np.float32) * 3
+    valid = np.array([L, 1, 2047, 2048, 2049, 50000])
+    assert _topk_case(s, valid, 2048) == 0
+
+
+def test_topk_ties_and_signed_zero():
+    rng = np.random.default_rng(1)
+    R, L = 5, 9000
+    s = np.zeros((R, L), dtype=np.float32)
+    s[1] = rng.integers(0, 3, L)               # heavy ties
+    s[2] = rng.integers(-2, 3, L).astype(np.float32) * 0.0  # +0 / -0 mix
+    s[3, :] = 1.0
+    s[3, ::7] = 2.0                             # 1286 twos, ties at the k-th place
+    s[4] = np.round(rng.standard_normal(L), 1)
+    valid = np.full(R, L)
+    assert _topk_case(s, valid, 2048) == 0
+    assert _topk_case(s, valid, 100, stride=4, offset=3) == 0
+
+
+def test_topk_nan_flag():
+    s = np.ones((1, 3000), dtype=np.float32)
+    s[0, 17] = np.nan
+    st = torch.from_numpy(s).to(DEV)
+    vt = torch.tensor([3000], dtype=torch.int32, device=DEV)
+    oi = torch.zeros((1, 64), dtype=torch.int32, device=DEV)
+    oc = torch.zeros(1, dtype=torch.int32, device=DEV)
+    err = _err()
+    api.dsa_topk(st, vt, 64, oi, oc, err)
+    assert api.dsa_read_error(err) & C.DSA_DEVERR_NAN
+
+
+def test_shard_merge_against_oracle():
+    rng = np.random.default_rng(2)
+    W, R, k, n = 3, 4, 256, 2000
+    cs = np.zeros((W, R, k), np.float32)
+    cp = np.full((W, R, k), -1, np.int32)
+    cc = np.zeros((W, R), np.int32)
+    s_full = rng.integers(0, 50, (R, n)).astype(np.float32)
+    for r in range(R):
+        for w in range(W):
+            pos = np.arange(w, n - r * 300, W)
+            j = orc.topk_select(s_full[r, pos].astype(np.float64), k)
+            cc[w, r] = len(j)
+            cs[w, r, : len(j)] = s_full[r, pos[j]]
+            cp[w, r, : len(j)] = pos[j]
+    t = lambda a: torch.from_numpy(a).to(DEV)  # noqa: E731
+    oi = torch.zeros((R, k), dtype=torch.int32, device=DEV)
+    oc = torch.zeros(R, dtype=torch.int32, device=DEV)
+    ol = torch.zeros((W, R, k), dtype=torch.int32, device=DEV)
+    ocnt = torch.zeros((W, R), dtype=torch.int32, device=DEV)
+    err = _err()
+    api.dsa_shard_topk_merge(t(cs), t(cp), t(cc), oi, oc, ol, ocnt, err)
+    assert api.dsa_read_error(err) == 0
+    for r in range(R):
+        sel, owned = orc.merge_candidates([cs[w, r, : cc[w, r]] for w in range(W)],
+                                          [cp[w, r, : cc[w, r]] for w in range(W)], k, W)
+        assert int(oc[r]) == len(sel)
+        assert np.array_equal(oi[r, : len(sel)].cpu().numpy(), sel)
+        for w in range(W):
+            m = int(ocnt[w, r])
+            assert np.array_equal(ol[w, r, :m].cpu().numpy(), owned[w])
+            assert np.all(ol[w, r, m:].cpu().numpy() == -1)
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_sparse_mla_alone(cfg):
+    wl = make_workload(config_spec(cfg, B=2, L=3000, L_lo=2500, L_hi=4000))
+    dw = upload(wl, DEV)
+    rng = np.random.default_rng(3)
+    k = 2048
+    idx = np.full((wl.R, k), -1, np.int32)
+    cnt = np.zeros(wl.R, np.int32)
+    for r in range(wl.R):
+        n = [2048, 5, 1, 700, 2048, 64, 65, 1000, 2048, 3, 128, 2000][r % 12]
+        n = min(n, int(wl.row_pos[r]) + 1)
+        idx[r, :n] = rng.choice(int(wl.row_pos[r]) + 1, n, replace=False)
+        cnt[r] = n
+    t = lambda a: torch.from_numpy(a).to(DEV)  # noqa: E731
+    for S in (0, 1, 3):
+        out = torch.zeros((wl.R, wl.H, 512), device=DEV)
+        lse = torch.zeros((wl.R, wl.H), device=DEV)
+        wsz = api.dsa_sparse_mla_decode_workspace_size(wl.R, wl.H, k, S)
+        ws = torch.zeros(max(wsz, 1), dtype=torch.uint8, device=DEV)
+        err = _err()
+        api.dsa_sparse_mla_decode(dw.q, wl.sm_scale, dw.kv, dw.rows, t(idx), t(cnt), out, lse,
+                                  err, workspace=ws, num_splits=S)
+        assert api.dsa_read_error(err) == 0
+        for r in range(wl.R):
+            O_ref, l_ref = orc.row_attention(wl, r, idx[r, : cnt[r]])
+            eo, el = attn_err(out[r].cpu().numpy(), lse[r].cpu().numpy(), O_ref, l_ref)
+            assert eo <= (2e-3 if cfg == 1 else 5e-3) and el <= 1e-4, (S, r, eo, el)
+
+
+def test_lse_merge_against_oracle():
+    rng = np.random.default_rng(4)
+    P, R, H, dv = 5, 3, 4, 512
+    Op = rng.standard_normal((P, R, H, dv)).astype(np.float32)
+    lp = (rng.standard_normal((P, R, H)) * 3).astype(np.float32)
+    lp[1, 0, :] = -np.inf
+    lp[:, 2, 1] = -np.inf  # a fully empty (row, head)
+    out = torch.zeros((R, H, dv), device=DEV)
+    ol = torch.zeros((R, H), device=DEV)
+    api.dsa_lse_merge(torch.from_numpy(Op).to(DEV), torch.from_numpy(lp).to(DEV), out, ol)
+    torch.cuda.synchronize()
+    for r in range(R):
+        O_ref, l_ref = orc.lse_merge(Op[:, r].astype(np.float64), lp[:, r].astype(np.float64))
+        assert np.allclose(out[r].cpu().numpy(), O_ref, rtol=1e-5, atol=1e-6)
+        got = ol[r].cpu().numpy()
+        assert np.array_equal(np.isneginf(got), np.isneginf(l_ref))
+        fin = np.isfinite(l_ref)
+        assert np.allclose(got[fin], l_ref[fin], atol=1e-5)
+
+
+# ------------------------------------------------------------- edge cases
+
+
+def test_single_token_rows():
+    """pos = 0: the only token is selected; O = its value, LSE = its logit."""
+    wl = make_workload(config_spec(1, B=3, L=1))
+    dw = upload(wl, DEV)
+    run = DecodeRun(dw)
+    assert run.run() == 0
+    check_decode_rows(run, range(wl.R))
+    assert np.all(run.cnt.cpu().numpy() == 1)
+
+
+def test_all_equal_scores_pick_first_positions():
+    wl = make_workload(config_spec(1, B=2, L=5000))
+    wl.idx_k.data[:] = 0  # every key 0 -> every score 0 -> ties everywhere
+    dw = upload(wl, DEV)
+    run = DecodeRun(dw)
+    assert run.run() == 0
+    idx = run.idx.cpu().numpy()
+    assert np.array_equal(idx[0], np.arange(2048)) and np.array_equal(idx[1], np.arange(2048))
+    check_decode_rows(run, range(wl.R))
+
+
+def test_bad_page_sets_error_bit():
+    wl = make_workload(config_spec(1, B=2, L=3000))
+    wl.idx_k.block_table = wl.idx_k.block_table.copy()
+    wl.idx_k.block_table[1, 3] = -1
+    dw = upload(wl, DEV)
+    run = DecodeRun(dw)
+    e = run.run()
+    assert e & C.DSA_DEVERR_PAGE
+
+
+def test_position_past_block_table_sets_error_bit():
+    wl = make_workload(config_spec(1, B=2, L=300))
+    wl.row_pos = wl.row_pos.copy()
+    wl.row_pos[0] = 64 * wl.idx_k.max_blocks + 5
+    dw = upload(wl, DEV)
+    run = DecodeRun(dw)
+    e = run.run()
+    assert e & C.DSA_DEVERR_POS
+
+
+def test_empty_batch_is_a_no_op():
+    wl = make_workload(config_spec(1, B=1, L=100))
+    dw = upload(wl, DEV)
+    dw.rows.row_pos = dw.rows.row_pos[:0]
+    dw.rows.row_start = torch.zeros(2, dtype=torch.int32, device=DEV)
+    out = torch.zeros((0, 32, 512), device=DEV)
+    lse = torch.zeros((0, 32), device=DEV)
+    d = api.DecodeDesc([dw.idx_k], [dw.kv], dw.rows, dw.q_idx, dw.w_idx, dw.q, wl.sm_scale,
+                       2048, out, lse)
+    ws = torch.zeros(max(1, api.dsa_decode_workspace_size(d)), dtype=torch.uint8, device=DEV)
+    api.dsa_decode(d, ws, _err())
+    torch.cuda.synchronize()
+
+
+def test_long_single_row_max_length():
+    """One 131072-token row (the longest cfg 4 length), fp8."""
+    wl = make_workload(config_spec(4, B=1, seq_lens=(131072,)))
+    dw = upload(wl, DEV)
+    run = DecodeRun(dw)
+    assert run.run() == 0
+    check_decode_rows(run, [0])
