@@ -187,7 +187,7 @@ def ncu_traffic(kernel: str):
 
 
 def algorithmic_bytes(wl):
-    """Bytes the method must move per step (what the design doc tabulates):
+    """Bytes the method must move per step:
     indexer key stream + block table + queries/weights; MLA selected rows +
     indices + query + output/LSE."""
     R, H = wl.R, wl.H

@@ -12,8 +12,8 @@
 // latent rows are gathered with 16-byte cp.async into a double buffer (fp8
 // rows are widened to f16 in shared memory: e4m3 values are f16 values) and
 // every head of the row shares each gathered tile:
-//   S = q . kv^T (all 576 dims), online softmax in fp32 (base 2), P rounded to
-//   the MMA input type, O += P . v (first 512 dims).
+//   S = q . kv^T (all 576 dims), online softmax in fp32 (base 2), P split into
+//   two bf16 parts (f16 for fp8 rows), O += P . v (first 512 dims).
 // The fp8 path multiplies each logit by the token's scale and folds the scale
 // into P for the value product; its query is converted to f16 with a per-head
 // power-of-two factor that the logit scale undoes.
@@ -50,7 +50,7 @@ __host__ __device__ inline MlaSmem mla_smem(int heads, int fp8, int chunk) {
   s.off_raw = off;
   off += fp8 ? 2 * kTile * kKvDim : 0;
   s.off_p = off;
-  off += heads * kPRowB;
+  off += (fp8 ? 1 : 2) * heads * kPRowB;  // bf16 path: P = hi + lo
   s.off_red = off;
   off += 2 * 8 * heads * 4;
   s.off_rowoff = off;
@@ -411,9 +411,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
           v10 *= k0;
           v11 *= k1;
         }
-        *reinterpret_cast<uint32_t*>(p_s + (mt_s * 16 + g) * kPRowB + tok * 2) = pack2<kFp8>(v00, v01);
-        *reinterpret_cast<uint32_t*>(p_s + (mt_s * 16 + g + 8) * kPRowB + tok * 2) =
-            pack2<kFp8>(v10, v11);
+        const uint32_t h0 = pack2<kFp8>(v00, v01), h1 = pack2<kFp8>(v10, v11);
+        *reinterpret_cast<uint32_t*>(p_s + (mt_s * 16 + g) * kPRowB + tok * 2) = h0;
+        *reinterpret_cast<uint32_t*>(p_s + (mt_s * 16 + g + 8) * kPRowB + tok * 2) = h1;
+        if (!kFp8) {
+          // bf16 keeps 8 significant bits: carry the rounding remainder of P
+          // in a second bf16 operand so that P . v is exact to ~2^-17
+          *reinterpret_cast<uint32_t*>(p_s + (H + mt_s * 16 + g) * kPRowB + tok * 2) =
+              pack2<false>(v00 - __uint_as_float(h0 << 16), v01 - __uint_as_float(h0 & 0xFFFF0000u));
+          *reinterpret_cast<uint32_t*>(p_s + (H + mt_s * 16 + g + 8) * kPRowB + tok * 2) =
+              pack2<false>(v10 - __uint_as_float(h1 << 16), v11 - __uint_as_float(h1 & 0xFFFF0000u));
+        }
       }
       l_part[0] = l_part[0] * alpha[mt_s][0] + ls0;
       l_part[1] = l_part[1] * alpha[mt_s][1] + ls1;
@@ -435,11 +443,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
       const int d0 = warp * 64;
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk) {
-        uint32_t af[MT][4];
+        uint32_t af[MT][4], al[MT][4];
 #pragma unroll
-        for (int a = 0; a < MT; ++a)
+        for (int a = 0; a < MT; ++a) {
           ldsm_x4(p_a + (a * 16 + (lane & 15)) * kPRowB + kk * 32 + (lane >> 4) * 16, af[a][0],
                   af[a][1], af[a][2], af[a][3]);
+          if (!kFp8)
+            ldsm_x4(p_a + (H + a * 16 + (lane & 15)) * kPRowB + kk * 32 + (lane >> 4) * 16,
+                    al[a][0], al[a][1], al[a][2], al[a][3]);
+        }
 #pragma unroll
         for (int j = 0; j < 8; j += 2) {
           uint32_t b0, b1, b2, b3;
@@ -450,6 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
           for (int a = 0; a < MT; ++a) {
             mma16816<kFp8>(o[a][j], af[a][0], af[a][1], af[a][2], af[a][3], b0, b1);
             mma16816<kFp8>(o[a][j + 1], af[a][0], af[a][1], af[a][2], af[a][3], b2, b3);
+            if (!kFp8) {
+              mma16816<false>(o[a][j], al[a][0], al[a][1], al[a][2], al[a][3], b0, b1);
+              mma16816<false>(o[a][j + 1], al[a][0], al[a][1], al[a][2], al[a][3], b2, b3);
+            }
           }
         }
       }

@@ -6,14 +6,16 @@
 //
 // One CTA of 1024 threads per score row:
 //   1. scores become order-preserving uint32 keys (-0 == +0), cached in shared
-//      memory when the row fits;
-//   2. radix select of the k-th largest key in three passes (11, 11, 10 bits)
-//      with shared-memory histograms fed by warp-aggregated atomics
-//      (__match_any_sync), which keeps the hot bins of similar scores cheap;
-//   3. keys above the threshold are appended; keys equal to it are taken in
-//      ascending position order (only the first ones needed);
-//   4. the k survivors are bitonic-sorted on (key, ~position) so the output
-//      order is score descending, then position ascending.
+//      memory when the row fits; the same pass builds a histogram of the top
+//      13 key bits;
+//   2. the bin holding the k-th largest key is refined with two more
+//      histograms (10 and 9 bits) over only the keys still in play, giving the
+//      exact threshold key T and how many keys equal to T are taken;
+//   3. keys above T are appended; keys equal to T are appended when all of
+//      them are taken, else the lowest positions are taken in position order;
+//   4. the k survivors are bitonic-sorted on (key, ~position) so that the
+//      output is ordered by score descending, then position ascending; the
+//      strides below 64 run in registers with warp shuffles.
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
 
@@ -23,45 +25,33 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kBins1 = 8192;  // key bits [31:19]
+constexpr int kShift1 = 19;
+constexpr int kShift2 = 9;    // key bits [18:9]
+constexpr int kBins2 = 1024;
+constexpr int kBins3 = 512;   // key bits [8:0]
 
 struct TopkSmem {
   int cap;         // keys cached in smem
-  int sort_n;      // power of two >= k
+  int sort_n;      // power of two >= max(k, 64)
   int off_keys, off_cand, off_hist, off_misc, total;
 };
 
-__host__ inline int pow2_at_least(int x) {
-  int p = 1;
-  while (p < x) p <<= 1;
-  return p;
-}
-
 __host__ inline TopkSmem topk_smem(int k) {
   TopkSmem s{};
-  s.sort_n = pow2_at_least(k);
-  const int cand = s.sort_n * 8;
-  const int hist = 2048 * 4;
-  const int misc = 1024;
+  int p = 64;
+  while (p < k) p <<= 1;
+  s.sort_n = p;
   s.off_cand = 0;
-  s.off_hist = cand;
-  s.off_misc = cand + hist;
-  s.off_keys = cand + hist + misc;
+  s.off_hist = s.sort_n * 8;
+  s.off_misc = s.off_hist + kBins1 * 4;
+  s.off_keys = s.off_misc + 1024;
   s.cap = ((kSmemLimit - s.off_keys) / 4) & ~1023;
   s.total = s.off_keys + s.cap * 4;
   return s;
 }
 
-__device__ __forceinline__ void agg_add(uint32_t* hist, bool active, uint32_t digit) {
-  const unsigned m = __ballot_sync(0xffffffffu, active);
-  if (active) {
-    const unsigned peers = __match_any_sync(m, digit);
-    if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(peers) - 1))
-      atomicAdd(hist + digit, static_cast<uint32_t>(__popc(peers)));
-  }
-}
-
-// inclusive suffix sums over the 1024 threads' values (sum of values of
-// threads >= tid); `scratch` holds 32 ints
+// inclusive suffix sum over the 1024 threads (sum of values of threads >= tid)
 __device__ __forceinline__ uint32_t block_suffix_sum(uint32_t v, uint32_t* scratch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t s = v;
@@ -78,6 +68,99 @@ __device__ __forceinline__ uint32_t block_suffix_sum(uint32_t v, uint32_t* scrat
   return s + add;
 }
 
+// Find the bin holding the k_rem-th largest key: writes (bin, k_rem within the
+// bin, bin count) to out[0..2].  Every thread calls it.
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, uint32_t k_rem,
+                                         uint32_t* scratch, uint32_t* out) {
+  const int per = nb / kThreads;  // >= 1 (nb is 8192, 1024 or 512 -> handle 512 below)
+  const int tid = threadIdx.x;
+  uint32_t mine = 0;
+  if (per >= 1) {
+    for (int j = 0; j < per; ++j) mine += hist[tid * per + j];
+  } else if (tid < nb) {
+    mine = hist[tid];
+  }
+  const uint32_t incl = block_suffix_sum(mine, scratch);
+  const uint32_t above = incl - mine;
+  if (above < k_rem && incl >= k_rem) {
+    const int p = per >= 1 ? per : 1;
+    uint32_t acc = above;
+    for (int j = p - 1; j >= 0; --j) {
+      const uint32_t h = hist[tid * p + j];
+      if (acc + h >= k_rem) {
+        out[0] = static_cast<uint32_t>(tid * p + j);
+        out[1] = k_rem - acc;
+        out[2] = h;
+        break;
+      }
+      acc += h;
+    }
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ uint64_t composite(uint32_t key, int i) {
+  return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~i);
+}
+
+// append the lanes' items with `pred` at buf[base + counter ...) (any order)
+__device__ __forceinline__ void warp_append(bool pred, uint64_t item, uint32_t* counter,
+                                            uint64_t* buf, uint32_t base) {
+  const int lane = threadIdx.x & 31;
+  const unsigned m = __ballot_sync(0xffffffffu, pred);
+  if (m == 0u) return;
+  const int leader = __ffs(m) - 1;
+  uint32_t b0 = 0;
+  if (lane == leader) b0 = atomicAdd(counter, static_cast<uint32_t>(__popc(m)));
+  b0 = __shfl_sync(0xffffffffu, b0, leader);
+  if (pred) buf[base + b0 + __popc(m & ((1u << lane) - 1u))] = item;
+}
+
+__device__ void bitonic_sort_desc(uint64_t* buf, int n) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int size = 2; size <= n; size <<= 1) {
+    int stride = size >> 1;
+    for (; stride >= 64; stride >>= 1) {
+      for (int t = tid; t < (n >> 1); t += kThreads) {
+        const int i = 2 * t - (t & (stride - 1));
+        const int j = i + stride;
+        const uint64_t a = buf[i], b = buf[j];
+        const bool desc = (i & size) == 0;
+        if (desc ? (a < b) : (a > b)) {
+          buf[i] = b;
+          buf[j] = a;
+        }
+      }
+      __syncthreads();
+    }
+    // strides < 64: chunks of 64 elements, two per lane, in registers
+    for (int c = warp; c < (n >> 6); c += kWarps) {
+      const int i0 = c * 64 + lane, i1 = i0 + 32;
+      uint64_t v0 = buf[i0], v1 = buf[i1];
+      for (int s = stride; s > 0; s >>= 1) {
+        if (s == 32) {
+          const bool desc = (i0 & size) == 0;
+          if (desc ? (v0 < v1) : (v0 > v1)) {
+            const uint64_t t = v0;
+            v0 = v1;
+            v1 = t;
+          }
+        } else {
+          const uint64_t o0 = __shfl_xor_sync(0xffffffffu, v0, s);
+          const uint64_t o1 = __shfl_xor_sync(0xffffffffu, v1, s);
+          const bool lower = (lane & s) == 0;
+          const bool d0 = (i0 & size) == 0, d1 = (i1 & size) == 0;
+          v0 = (lower == d0) ? (v0 > o0 ? v0 : o0) : (v0 < o0 ? v0 : o0);
+          v1 = (lower == d1) ? (v1 > o1 ? v1 : o1) : (v1 < o1 ? v1 : o1);
+        }
+      }
+      buf[i0] = v0;
+      buf[i1] = v1;
+    }
+    __syncthreads();
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     topk_kernel(const TopkLaunch P, const TopkSmem S) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -85,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + S.off_hist);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + S.off_misc);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + S.off_keys);
-  uint32_t* scratch = misc;            // 32 words
-  uint32_t* sh = misc + 64;            // shared scalars
+  uint32_t* scratch = misc;       // 32 words
+  uint32_t* sh = misc + 64;       // shared scalars
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -108,18 +191,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* src = P.scores + static_cast<long long>(w) * P.shard_stride +
                      static_cast<long long>(r) * P.ld;
   const bool in_smem = n <= S.cap;
+  const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+  const int cnt = n < k ? n : k;
+  int sort_n = 64;
+  while (sort_n < cnt) sort_n <<= 1;
 
-  if (tid == 0) {
-    sh[0] = 0;  // NaN seen
-    sh[1] = 0;  // append counter (above threshold)
-    sh[2] = 0;  // append counter (equal to threshold)
-  }
-  // load keys (and check NaN)
+  for (int b = tid; b < kBins1; b += kThreads) hist[b] = 0;
+  if (tid < 16) sh[tid] = 0;
+  __syncthreads();
+
+  // ---------------- pass 1: keys (+ smem copy) and the 13-bit histogram
+  const bool need_select = n > k;
   bool nan_seen = false;
-  for (int i = tid; i < n; i += kThreads) {
-    const float f = __ldg(src + i);
-    nan_seen |= (f != f);
-    if (in_smem) keys[i] = score_key(f);
+  {
+    const int nv = vec ? (n >> 2) : 0;
+    const float4* src4 = reinterpret_cast<const float4*>(src);
+    for (int base = 0; base < nv; base += kThreads * 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * kThreads + tid;
+        v[u] = i < nv ? __ldg(src4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * kThreads + tid;
+        if (i < nv) {
+          const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          uint4 kk;
+          uint32_t* kp = reinterpret_cast<uint32_t*>(&kk);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            nan_seen |= (f[e] != f[e]);
+            kp[e] = score_key(f[e]);
+            if (need_select) atomicAdd(hist + (kp[e] >> kShift1), 1u);
+          }
+          if (in_smem) reinterpret_cast<uint4*>(keys)[i] = kk;
+        }
+      }
+    }
+    for (int i = nv * 4 + tid; i < n; i += kThreads) {
+      const float f = __ldg(src + i);
+      nan_seen |= (f != f);
+      const uint32_t key = score_key(f);
+      if (need_select) atomicAdd(hist + (key >> kShift1), 1u);
+      if (in_smem) keys[i] = key;
+    }
   }
   if (nan_seen) sh[0] = 1;
   __syncthreads();
@@ -129,99 +246,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     return in_smem ? keys[i] : score_key(__ldg(src + i));
   };
 
-  const int cnt = n < k ? n : k;
-  int sort_n = 1;
-  while (sort_n < cnt) sort_n <<= 1;
-
-  if (n <= k) {
-    for (int i = tid; i < sort_n; i += kThreads)
-      cand[i] = i < n ? ((static_cast<uint64_t>(key_at(i)) << 32) | static_cast<uint32_t>(~i))
-                      : 0ull;
+  if (!need_select) {
+    for (int i = tid; i < sort_n; i += kThreads) cand[i] = i < n ? composite(key_at(i), i) : 0ull;
   } else {
-    // ---------------- radix select of the k-th largest key
-    uint32_t prefix = 0, pmask = 0;
-    uint32_t k_rem = static_cast<uint32_t>(k);
-    uint32_t eq_count = 0;
-    const int shifts[3] = {21, 10, 0};
-    const int widths[3] = {11, 11, 10};
-    for (int pass = 0; pass < 3; ++pass) {
-      const int shift = shifts[pass];
-      const int nb = 1 << widths[pass];
-      const uint32_t dmask = static_cast<uint32_t>(nb - 1);
-      for (int b = tid; b < nb; b += kThreads) hist[b] = 0;
-      __syncthreads();
-      for (int base = 0; base < n; base += kThreads) {
-        const int i = base + tid;
-        uint32_t key = 0;
-        bool act = false;
-        if (i < n) {
-          key = key_at(i);
-          act = (key & pmask) == prefix;
-        }
-        agg_add(hist, act, (key >> shift) & dmask);
-      }
-      __syncthreads();
-      // thread t owns bins [t*per, (t+1)*per); find the bin where the count
-      // of keys >= bin reaches k_rem
-      const int per = nb / kThreads;  // 2 or 1
-      uint32_t mine = 0;
-      for (int j = 0; j < per; ++j) mine += hist[tid * per + j];
-      const uint32_t incl = block_suffix_sum(mine, scratch);
-      const uint32_t above = incl - mine;  // keys in bins above my range
-      if (above < k_rem && incl >= k_rem) {
-        uint32_t acc = above;
-        for (int j = per - 1; j >= 0; --j) {
-          const uint32_t h = hist[tid * per + j];
-          if (acc + h >= k_rem) {
-            sh[4] = static_cast<uint32_t>(tid * per + j);
-            sh[5] = k_rem - acc;
-            sh[6] = h;
-            break;
-          }
-          acc += h;
-        }
-      }
-      __syncthreads();
-      prefix |= sh[4] << shift;
-      pmask |= dmask << shift;
-      k_rem = sh[5];
-      eq_count = sh[6];
-      __syncthreads();
+    // ---------------- refine the threshold bin to the exact k-th key
+    find_bin(hist, kBins1, static_cast<uint32_t>(k), scratch, sh + 4);
+    const uint32_t b1 = sh[4];
+    uint32_t k_rem = sh[5];
+    for (int b = tid; b < kBins2; b += kThreads) hist[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+      const uint32_t key = key_at(i);
+      if ((key >> kShift1) == b1) atomicAdd(hist + ((key >> kShift2) & (kBins2 - 1)), 1u);
     }
-    const uint32_t T = prefix;
+    __syncthreads();
+    find_bin(hist, kBins2, k_rem, scratch, sh + 4);
+    const uint32_t pre2 = (b1 << (kShift1 - kShift2)) | sh[4];
+    k_rem = sh[5];
+    for (int b = tid; b < kBins3; b += kThreads) hist[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kThreads) {
+      const uint32_t key = key_at(i);
+      if ((key >> kShift2) == pre2) atomicAdd(hist + (key & (kBins3 - 1)), 1u);
+    }
+    __syncthreads();
+    find_bin(hist, kBins3, k_rem, scratch, sh + 4);
+    const uint32_t T = (pre2 << kShift2) | sh[4];
+    k_rem = sh[5];
+    const uint32_t eq_count = sh[6];
     const uint32_t n_gt = static_cast<uint32_t>(k) - k_rem;
     const bool take_all_eq = eq_count == k_rem;
-    // ---------------- collect: keys > T anywhere in [0, n_gt); keys == T
+    __syncthreads();
+
+    // ---------------- collect
     for (int base = 0; base < n; base += kThreads) {
       const int i = base + tid;
-      uint32_t key = 0;
-      if (i < n) key = key_at(i);
-      const bool gt = i < n && key > T;
-      const bool eq = i < n && key == T && take_all_eq;
-      {
-        const unsigned m = __ballot_sync(0xffffffffu, gt);
-        if (m) {
-          uint32_t b0 = 0;
-          if (lane == __ffs(m) - 1) b0 = atomicAdd(sh + 1, static_cast<uint32_t>(__popc(m)));
-          b0 = __shfl_sync(0xffffffffu, b0, __ffs(m) - 1);
-          if (gt) {
-            const uint32_t pos = b0 + __popc(m & ((1u << lane) - 1u));
-            cand[pos] = (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~i);
-          }
-        }
-      }
-      {
-        const unsigned m = __ballot_sync(0xffffffffu, eq);
-        if (m) {
-          uint32_t b0 = 0;
-          if (lane == __ffs(m) - 1) b0 = atomicAdd(sh + 2, static_cast<uint32_t>(__popc(m)));
-          b0 = __shfl_sync(0xffffffffu, b0, __ffs(m) - 1);
-          if (eq) {
-            const uint32_t pos = n_gt + b0 + __popc(m & ((1u << lane) - 1u));
-            cand[pos] = (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~i);
-          }
-        }
-      }
+      const uint32_t key = i < n ? key_at(i) : 0u;
+      warp_append(i < n && key > T, composite(key, i), sh + 1, cand, 0u);
+      if (take_all_eq) warp_append(i < n && key == T, composite(key, i), sh + 2, cand, n_gt);
     }
     if (!take_all_eq) {
       // ties at the threshold: the k_rem lowest positions, in position order
@@ -240,8 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (eq) {
           const uint32_t rank = taken + off + __popc(m & ((1u << lane) - 1u));
-          if (rank < k_rem)
-            cand[n_gt + rank] = (static_cast<uint64_t>(T) << 32) | static_cast<uint32_t>(~i);
+          if (rank < k_rem) cand[n_gt + rank] = composite(T, i);
         }
         taken += tot;
         __syncthreads();
@@ -251,22 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  // ---------------- bitonic sort, descending
-  for (int size = 2; size <= sort_n; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = tid; t < (sort_n >> 1); t += kThreads) {
-        const int i = 2 * t - (t & (stride - 1));
-        const int j = i + stride;
-        const uint64_t a = cand[i], b = cand[j];
-        const bool desc = (i & size) == 0;
-        if (desc ? (a < b) : (a > b)) {
-          cand[i] = b;
-          cand[j] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
+  bitonic_sort_desc(cand, sort_n);
 
   // ---------------- write
   const int off = P.index_offset + (P.offset_per_shard ? (w + P.shard_offset) : 0);
