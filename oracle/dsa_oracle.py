@@ -26,9 +26,9 @@ design notes):
 * fp8 caches: stored value = e4m3 code value * per-token fp32 scale;
 * attention logits ``z_t = tau * (q . kv_t)`` over all 576 latent dims with
   ``tau = 1/sqrt(576)``; the value vector is the first 512 dims of the same row;
-* ordering of the selection: score descending, then token position ascending;
-  the output list is in that order; with fewer valid tokens than k all of them
-  are kept;
+* selection order: score descending, then token position ascending (a tie
+  at the k-th place goes to the lower position); the selected positions are
+  listed in ascending order; with fewer valid tokens than k all are kept;
 * a row at position ``pos`` sees tokens 0..pos;
 * an empty partial (no tokens) has LSE = -inf and contributes nothing.
 
@@ -127,15 +127,16 @@ def topk_select(scores: np.ndarray, k: int, positions: Optional[np.ndarray] = No
                 ) -> np.ndarray:
     """Exact top-k (DCP page, Motivation: "the top 2048 tokens of the whole
     sequence").  Full sort by score descending, then position ascending; the
-    first min(k, n) entries, in that order.  Returns the positions (defaults
-    to 0..n-1)."""
+    first min(k, n) entries are the selection.  The pages fix which tokens
+    are kept, not the order of the list: it is reported in ascending position
+    order.  Returns the positions (default positions 0..n-1)."""
     s = np.asarray(scores, dtype=np.float64)
     if np.any(np.isnan(s)):
         raise ValueError("NaN score")
     n = s.shape[0]
     pos = np.arange(n, dtype=np.int64) if positions is None else np.asarray(positions, dtype=np.int64)
     order = np.lexsort((pos, -s))           # last key is the primary key
-    return pos[order[: min(k, n)]]
+    return np.sort(pos[order[: min(k, n)]])
 
 
 # ----------------------------------------------------------------------------

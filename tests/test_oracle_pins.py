@@ -128,7 +128,7 @@ def test_indexer_closed_forms():
 
 
 def _brute_topk(s, k):
-    return [t for _, t in sorted(((-float(v), t) for t, v in enumerate(s)))][:k]
+    return sorted([t for _, t in sorted(((-float(v), t) for t, v in enumerate(s)))][:k])
 
 
 @pytest.mark.parametrize("seed", range(12))
@@ -143,13 +143,16 @@ def test_topk_brute_force_with_ties(seed):
 def test_topk_special_cases():
     assert orc.topk_select(np.zeros(5000), 2048).tolist() == list(range(2048))
     s = np.array([3.0, 1.0, 2.0])
-    assert orc.topk_select(s, 2048).tolist() == [0, 2, 1]
+    assert orc.topk_select(s, 2048).tolist() == [0, 1, 2]
+    assert orc.topk_select(s, 2).tolist() == [0, 2]
     # ties straddling the k-th place: the lower positions win
     s = np.array([1.0, 5.0, 2.0, 2.0, 2.0, 0.0])
     assert orc.topk_select(s, 3).tolist() == [1, 2, 3]
+    s = np.array([2.0, 5.0, 2.0, 9.0, 2.0, 0.0])
+    assert orc.topk_select(s, 3).tolist() == [0, 1, 3]
     # -0.0 and +0.0 are the same score
     s = np.array([-0.0, 0.0, -0.0, 1.0])
-    assert orc.topk_select(s, 3).tolist() == [3, 0, 1]
+    assert orc.topk_select(s, 3).tolist() == [0, 1, 3]
     with pytest.raises(ValueError):
         orc.topk_select(np.array([1.0, np.nan]), 1)
 
