@@ -7,8 +7,8 @@ top-2048, 64-token pages with seeded random block tables (synthetic data).
 
 A step is one dsa_decode call (indexer -> top-k -> sparse MLA split-K ->
 LSE merge) over the whole batch, inputs resident in HBM.  Between timed steps
-L2 is flushed by writing a 512 MB buffer (the step's own HBM stream, ~350 MB,
-is also larger than L2).  Each step is timed with CUDA events on the launching
+L2 is flushed by writing a 512 MB buffer and then reading a 256 MB one (the
+step's own HBM stream, ~350 MB, is also larger than L2).  Each step is timed with CUDA events on the launching
 stream; `value` = rows of all ranks / max over ranks of the summed step time.
 
 `--impl reference` times the CPU oracle instead (the only other place that
@@ -239,8 +239,15 @@ def run_product(args):
     lay = api.dsa_decode_workspace_layout(desc)
     ws = torch.zeros(lay.total_bytes, dtype=torch.uint8, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
+
+    def flush_l2():
+        # write 512 MB (> L2), then read 256 MB so that L2 is left holding clean
+        # lines: no write-back of the flush competes with the next timed kernel
+        flush_w.zero_()
+        flush_r.sum()
 
     def step():
         api.dsa_decode(desc, ws, err, stream=stream)
@@ -255,7 +262,7 @@ def run_product(args):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(n)]
         for a, b in evs:
-            flush.zero_()
+            flush_l2()
             a.record(stream)
             fn()
             b.record(stream)
@@ -349,7 +356,7 @@ def run_product(args):
             "data": "synthetic (seeded N(0,1)/N(0,0.5) bf16 caches and queries, U(0,1)/8 weights)",
             "config": {"workload": WORKLOAD, "global_batch": R * world, "seq_len": 32768,
                        "topk": k, "mla_heads": H, "num_splits": lay.num_splits,
-                       "l2": "flushed between timed steps (512 MB write); step stream ~350 MB > L2",
+                       "l2": "flushed between timed steps (512 MB write, then 256 MB read); step stream ~350 MB > L2",
                        "parallelism": f"dp{world} (independent request batches per GPU)"},
             "roofline": roofline,
             "kernels_us": {n: round(v, 2) for n, v in kern_us.items()},

@@ -224,7 +224,7 @@ int dsa_shard_topk_merge(const float* cand_score, const int32_t* cand_pos,
   if (num_shards < 1 || num_shards > kMaxShards || num_rows < 0 || k < 1 || k > 4096 ||
       d_err == nullptr)
     return DSA_ERR_INVALID_ARG;
-  if (merge_smem_bytes(num_shards, k) > 220 * 1024) return DSA_ERR_UNSUPPORTED;
+  if (merge_smem_bytes(num_shards, k) > 227 * 1024) return DSA_ERR_UNSUPPORTED;
   if (num_rows == 0) return DSA_OK;
   if (!cand_score || !cand_pos || !cand_count || !out_idx || !out_count || !owned_local ||
       !owned_count)
@@ -328,7 +328,7 @@ static int check_decode(const dsa_decode_desc* d) {
   }
   if (d->heads != 16 && d->heads != 32) return DSA_ERR_UNSUPPORTED;
   if (d->topk < 1 || d->topk > 4096 || d->num_splits < 0) return DSA_ERR_INVALID_ARG;
-  if (d->num_shards > 1 && merge_smem_bytes(d->num_shards, d->topk) > 220 * 1024)
+  if (d->num_shards > 1 && merge_smem_bytes(d->num_shards, d->topk) > 227 * 1024)
     return DSA_ERR_UNSUPPORTED;
   if (d->rows.num_rows > 0) {
     if (!d->q_idx || !d->w_idx || !d->q || !d->out || !d->out_lse) return DSA_ERR_INVALID_ARG;

@@ -8,31 +8,85 @@
 // same LSE merge also combines split-K partials.
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
+#include "dsa_select.cuh"
 
 namespace dsa {
 namespace {
 
 // ------------------------------------------------------------ top-k merge
 //
-// Every candidate's place in the merged order is its index in its own list
-// plus, for every other list, the number of entries that precede it there
-// (binary search: lists are sorted by score descending, position ascending;
-// positions of different shards differ, so there are no exact ties).
-constexpr int kMergeThreads = 1024;
+// The global top-k is the top-k of the union of the shards' candidate lists
+// (every token of the global top-k is in its own shard's local top-k).  One
+// 1024-thread CTA per query row:
+//   1. the exact threshold key T over the union (histograms, as for one row),
+//      ties at T going to the lowest global positions;
+//   2. a candidate's rank among the ties, and later its output slot, is the
+//      number of tied (selected) candidates with a lower global position in
+//      every list: per-list prefix counts + a binary search in each list,
+//      whose positions ascend;
+//   3. selected positions go to the global list in ascending order and, as
+//      local positions (p / W), to their own shard's owned list.
+constexpr int kMergeThreads = kSelThreads;
 
-__device__ __forceinline__ bool precedes(float as, int ap, float bs, int bp) {
-  return as > bs || (as == bs && ap < bp);
+struct MergeSmem {
+  int off_keys, off_pos, off_pre, off_hist, off_misc, total;
+};
+
+__host__ __device__ inline MergeSmem merge_smem(int W, int k) {
+  MergeSmem m{};
+  const int N = W * k;
+  m.off_keys = 0;
+  m.off_pos = N * 4;
+  m.off_pre = 2 * N * 4;
+  m.off_hist = 3 * N * 4;
+  m.off_misc = m.off_hist + kSelBins1 * 4;
+  m.total = m.off_misc + 1024;
+  return m;
+}
+
+// exclusive prefix of flag(e) over list w's first cnt entries -> pre[w*k + i];
+// returns the list total.  Called by one whole warp.
+template <class FlagFn>
+__device__ __forceinline__ uint32_t warp_list_prefix(FlagFn flag, int w, int k, int cnt,
+                                                     uint32_t* pre) {
+  const int lane = threadIdx.x & 31;
+  uint32_t run = 0;
+  for (int i0 = 0; i0 < cnt; i0 += 32) {
+    const int i = i0 + lane;
+    const bool f = i < cnt && flag(w * k + i);
+    const unsigned m = __ballot_sync(0xffffffffu, f);
+    if (i < cnt) pre[w * k + i] = run + __popc(m & ((1u << lane) - 1u));
+    run += __popc(m);
+  }
+  return run;
+}
+
+// number of entries of ascending list [p0, p0 + n) below x
+__device__ __forceinline__ int lower_bound(const int* a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] < x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
 }
 
 __global__ void __launch_bounds__(kMergeThreads, 1) shard_topk_merge_kernel(const MergeTopkLaunch P) {
   extern __shared__ __align__(16) uint8_t smem[];
-  const int W = P.W, k = P.k, R = P.rows;
-  float* cs = reinterpret_cast<float*>(smem);
-  int* cp = reinterpret_cast<int*>(smem + static_cast<size_t>(W) * k * 4);
-  int* cnt = reinterpret_cast<int*>(smem + static_cast<size_t>(W) * k * 8);
-  int* owned = cnt + DSA_MAX_SHARDS;
+  const int W = P.W, k = P.k, R = P.rows, N = W * k;
+  const MergeSmem S = merge_smem(W, k);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + S.off_keys);  // later: selected flags
+  int* pos = reinterpret_cast<int*>(smem + S.off_pos);
+  uint32_t* pre = reinterpret_cast<uint32_t*>(smem + S.off_pre);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + S.off_hist);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + S.off_misc);
+  uint32_t* scratch = misc;                             // 32
+  uint32_t* sh = misc + 32;                             // 8
+  int* cnt = reinterpret_cast<int*>(misc + 64);         // [8]
+  uint32_t* tot = misc + 80;                            // [8] per-list totals
   const int r = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5;
 
   if (tid < W) {
     int c = P.cand_count[tid * R + r];
@@ -41,55 +95,90 @@ __global__ void __launch_bounds__(kMergeThreads, 1) shard_topk_merge_kernel(cons
       c = c < 0 ? 0 : k;
     }
     cnt[tid] = c;
-    owned[tid] = 0;
   }
-  __syncthreads();
-  for (int e = tid; e < W * k; e += kMergeThreads) {
-    const int w = e / k, i = e - w * k;
-    if (i < cnt[w]) {
-      cs[e] = P.cand_score[(static_cast<long long>(w) * R + r) * k + i];
-      cp[e] = P.cand_pos[(static_cast<long long>(w) * R + r) * k + i];
-    }
-  }
+  for (int b = tid; b < kSelBins1; b += kMergeThreads) hist[b] = 0;
   __syncthreads();
   int total = 0;
-  for (int w = 0; w < W; ++w) total += cnt[w];
-  const int out_cnt = total < k ? total : k;
-
-  int32_t* oidx = P.out_idx + static_cast<long long>(r) * k;
-  for (int e = tid; e < W * k; e += kMergeThreads) {
+  for (int v = 0; v < W; ++v) total += cnt[v];
+  const bool all = total <= k;
+  auto valid = [&](int e) { return (e % k) < cnt[e / k]; };
+  for (int e = tid; e < N; e += kMergeThreads) {
     const int w = e / k, i = e - w * k;
-    if (i >= cnt[w]) continue;
-    const float s = cs[e];
-    const int p = cp[e];
-    if (p < 0 || p % W != w) raise_err(P.d_err, DSA_DEVERR_INDEX);
-    int rank = i;
-    for (int v = 0; v < W; ++v) {
-      if (v == w) continue;
-      int lo = 0, hi = cnt[v];  // first entry of list v that does not precede (s, p)
-      const float* vs = cs + v * k;
-      const int* vp = cp + v * k;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (precedes(vs[mid], vp[mid], s, p)) lo = mid + 1;
-        else hi = mid;
-      }
-      rank += lo;
-    }
-    if (rank < k) {
-      oidx[rank] = p;
-      P.owned_local[(static_cast<long long>(w) * R + r) * k + i] = p / W;
-      atomicAdd(owned + w, 1);
+    if (i < cnt[w]) {
+      const long long g = (static_cast<long long>(w) * R + r) * k + i;
+      const uint32_t key = score_key(P.cand_score[g]);
+      const int p = P.cand_pos[g];
+      if (p < 0 || p % W != w) raise_err(P.d_err, DSA_DEVERR_INDEX);
+      keys[e] = key;
+      pos[e] = p;
+      if (!all) atomicAdd(hist + (key >> kSelShift1), 1u);
     }
   }
   __syncthreads();
-  for (int j = out_cnt + tid; j < k; j += kMergeThreads) oidx[j] = -1;
-  for (int e = tid; e < W * k; e += kMergeThreads) {
-    const int w = e / k, i = e - w * k;
-    if (i >= owned[w]) P.owned_local[(static_cast<long long>(w) * R + r) * k + i] = -1;
+  uint32_t T = 0, k_rem = 0;
+  if (!all)
+    refine_threshold([&](int e) { return keys[e]; }, valid, N, static_cast<uint32_t>(k), hist,
+                     scratch, sh, T, k_rem);
+
+  // ranks of the ties at T, by global position
+  if (warp < W) {
+    const uint32_t t =
+        warp_list_prefix([&](int e) { return !all && keys[e] == T; }, warp, k, cnt[warp], pre);
+    if ((tid & 31) == 0) tot[warp] = t;
   }
-  if (tid < W) P.owned_count[tid * R + r] = owned[tid];
-  if (tid == 0) P.out_count[r] = out_cnt;
+  __syncthreads();
+  uint32_t selflag[(DSA_MAX_SHARDS * 4096 + kMergeThreads - 1) / kMergeThreads];
+  for (int e = tid, it = 0; e < N; e += kMergeThreads, ++it) {
+    const int w = e / k, i = e - w * k;
+    bool sel = false;
+    if (i < cnt[w]) {
+      const uint32_t key = keys[e];
+      if (all || key > T) {
+        sel = true;
+      } else if (key == T) {
+        uint32_t rank = pre[e];
+        for (int v = 0; v < W; ++v) {
+          if (v == w) continue;
+          const int j = lower_bound(pos + v * k, cnt[v], pos[e]);
+          rank += j < cnt[v] ? pre[v * k + j] : tot[v];
+        }
+        sel = rank < k_rem;
+      }
+    }
+    selflag[it] = sel ? 1u : 0u;
+  }
+  __syncthreads();
+  for (int e = tid, it = 0; e < N; e += kMergeThreads, ++it) keys[e] = selflag[it];
+  __syncthreads();
+  // output slots: selected candidates with a lower global position
+  if (warp < W) {
+    const uint32_t t = warp_list_prefix([&](int e) { return keys[e] != 0u; }, warp, k, cnt[warp], pre);
+    if ((tid & 31) == 0) tot[warp] = t;
+  }
+  __syncthreads();
+  uint32_t out_cnt = 0;
+  for (int v = 0; v < W; ++v) out_cnt += tot[v];
+  int32_t* oidx = P.out_idx + static_cast<long long>(r) * k;
+  for (int e = tid; e < N; e += kMergeThreads) {
+    const int w = e / k, i = e - w * k;
+    if (i >= cnt[w] || keys[e] == 0u) continue;
+    const int p = pos[e];
+    uint32_t slot = pre[e];
+    for (int v = 0; v < W; ++v) {
+      if (v == w) continue;
+      const int j = lower_bound(pos + v * k, cnt[v], p);
+      slot += j < cnt[v] ? pre[v * k + j] : tot[v];
+    }
+    oidx[slot] = p;
+    P.owned_local[(static_cast<long long>(w) * R + r) * k + pre[e]] = p / W;
+  }
+  for (int j = static_cast<int>(out_cnt) + tid; j < k; j += kMergeThreads) oidx[j] = -1;
+  for (int e = tid; e < N; e += kMergeThreads) {
+    const int w = e / k, i = e - w * k;
+    if (i >= static_cast<int>(tot[w])) P.owned_local[(static_cast<long long>(w) * R + r) * k + i] = -1;
+  }
+  if (tid < W) P.owned_count[tid * R + r] = static_cast<int>(tot[tid]);
+  if (tid == 0) P.out_count[r] = static_cast<int>(out_cnt);
 }
 
 // ------------------------------------------------------------ LSE merge
@@ -131,7 +220,7 @@ __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
 
 }  // namespace
 
-int merge_smem_bytes(int W, int k) { return W * k * 8 + 2 * DSA_MAX_SHARDS * 4; }
+int merge_smem_bytes(int W, int k) { return merge_smem(W, k).total; }
 
 cudaError_t launch_shard_topk_merge(const MergeTopkLaunch& p, cudaStream_t stream) {
   if (p.rows == 0) return cudaSuccess;

@@ -25,9 +25,11 @@
  *
  * Readings of points the pages leave open (fixed by this library):
  *   - indexer: 64 heads x 128 dims, score(t) = sum_h w[h] * relu(q[h] . k[t]);
- *   - selection order: score descending, then token position ascending; the
- *     index list is written in that order; rows with fewer visible tokens than
- *     k keep all of them and pad the list with -1;
+ *   - selection: the k tokens first in the order (score descending, token
+ *     position ascending), so a tie at the k-th place goes to the lower
+ *     position; the selected positions are written in ascending order (the
+ *     pages fix which tokens are kept, not the order of the list); rows with
+ *     fewer visible tokens than k keep all of them and pad the list with -1;
  *   - MLA latent rows are 576 wide; logits z = sm_scale * (q . kv) over all
  *     576 dims; the value is the first 512 dims of the same row;
  *   - fp8 caches hold OCP E4M3 codes with one fp32 scale per token
@@ -193,9 +195,10 @@ int dsa_indexer_scores(const uint16_t* q_idx, const float* w_idx,
  *              valid entries
  *   valid_len: device int32 [num_rows], 0 <= valid_len[r] <= ld_scores
  *   k:         1..4096
- *   out_idx:   device int32 [num_rows][k]: the selected j, mapped to
- *              j * index_stride + index_offset, in the order (score desc,
- *              j asc); entries past out_count[r] are -1
+ *   out_idx:   device int32 [num_rows][k]: the selected j (the k first in
+ *              the order score desc, j asc), mapped to j * index_stride +
+ *              index_offset, listed by ascending j; entries past
+ *              out_count[r] are -1
  *   out_score: device fp32 [num_rows][k] or NULL: the selected scores, same
  *              order (entries past the count are -inf)
  *   out_count: device int32 [num_rows]: min(k, valid_len[r])
@@ -214,15 +217,16 @@ int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* valid_len,
  * Modifications / Indexer decode: the all-gathered (score, global position)
  * candidates are merged and the merge emits the local rows every shard owns).
  *
- *   cand_score: device fp32 [W][num_rows][k], each list sorted by (score
- *               desc, position asc) as dsa_topk writes it
- *   cand_pos:   device int32 [W][num_rows][k] global positions; shard w's
- *               positions are == w mod W
+ *   cand_score: device fp32 [W][num_rows][k]: each shard's local top-k
+ *               scores, listed by ascending position as dsa_topk writes them
+ *   cand_pos:   device int32 [W][num_rows][k] global positions (ascending in
+ *               each list); shard w's positions are == w mod W
  *   cand_count: device int32 [W][num_rows]
- *   out_idx:    device int32 [num_rows][k] global top-k (same order), -1 pad
+ *   out_idx:    device int32 [num_rows][k] global top-k of the union (ties at
+ *               the k-th place to the lower position), ascending, -1 pad
  *   out_count:  device int32 [num_rows] = min(k, sum_w cand_count)
  *   owned_local: device int32 [W][num_rows][k]: local positions (pos / W) of
- *               the selected tokens shard w owns, in selection order, -1 pad
+ *               the selected tokens shard w owns, ascending, -1 pad
  *   owned_count: device int32 [W][num_rows]
  */
 int dsa_shard_topk_merge(const float* cand_score, const int32_t* cand_pos,
