@@ -32,6 +32,7 @@ INDEX_DIM = 128
 KV_DIM = 576
 V_DIM = 512
 MAX_SHARDS = 8
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class DsaPagedCache(ctypes.Structure):
@@ -113,6 +114,9 @@ PROTOTYPES = {
                                       POINTER(DsaRows), c_void_p, c_void_p, c_int32, c_int32,
                                       c_void_p, c_void_p, c_void_p, c_size_t, c_void_p,
                                       c_void_p]),
+    "dsa_sparse_mla_decode_noalloc": (c_int, [c_void_p, c_int32, c_float, POINTER(DsaPagedCache),
+                                              POINTER(DsaRows), c_void_p, c_void_p, c_int32,
+                                              c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dsa_lse_merge": (c_int, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p,
                               c_void_p, c_void_p]),
     "dsa_decode_workspace_size": (c_size_t, [POINTER(DsaDecodeDesc)]),

@@ -139,6 +139,20 @@ def dsa_sparse_mla_decode(q, sm_scale: float, kv: PagedCache, rows: Rows, idx, c
            "dsa_sparse_mla_decode")
 
 
+def dsa_sparse_mla_decode_noalloc(q, sm_scale: float, kv: PagedCache, rows: Rows, idx, count,
+                                  out, out_lse, d_err, num_splits: int = 0, stream=None):
+    """dsa_sparse_mla_decode for callers that cannot allocate device memory:
+    the split-K partials live in the library's fixed device array (see the
+    header); calls that overlap on the GPU race on it."""
+    c, r = kv.c(), rows.c()
+    k = int(idx.shape[1])
+    _check(C.lib().dsa_sparse_mla_decode_noalloc(_ptr(q), int(q.shape[1]), float(sm_scale),
+                                                 ctypes.byref(c), ctypes.byref(r), _ptr(idx),
+                                                 _ptr(count), k, num_splits, _ptr(out),
+                                                 _ptr(out_lse), _ptr(d_err), _stream(stream)),
+           "dsa_sparse_mla_decode_noalloc")
+
+
 def dsa_lse_merge(O_parts, lse_parts, out, out_lse, stream=None):
     P, R, H, dv = (int(x) for x in O_parts.shape)
     _check(C.lib().dsa_lse_merge(_ptr(O_parts), _ptr(lse_parts), P, R, H, dv, _ptr(out),

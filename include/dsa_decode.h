@@ -270,6 +270,39 @@ int dsa_sparse_mla_decode(const uint16_t* q, int32_t heads, float sm_scale,
                           int32_t* d_err, void* stream);
 
 /*
+ * Size of the fixed device array behind dsa_sparse_mla_decode_noalloc.
+ */
+#define DSA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * dsa_sparse_mla_decode_noalloc -- dsa_sparse_mla_decode without a caller
+ * workspace, for callers that cannot allocate device memory (a serving
+ * runtime that reserved nearly all HBM for its KV pools, a plugin whose host
+ * framework owns every allocation, a path where a synchronizing
+ * cudaMalloc/cudaFree is not affordable).  The pages have no counterpart of
+ * this entry point; it is a convenience of this library.
+ *
+ * Same arguments, results and errors as dsa_sparse_mla_decode.  The split-K
+ * partials go to one fixed device array of DSA_NOALLOC_SCRATCH_BYTES that the
+ * library image carries: every GPU that loads the library holds it until the
+ * process exits, and the call never allocates or frees device memory.
+ *   - Sizes whose partials do not fit (dsa_sparse_mla_decode_workspace_size()
+ *     > DSA_NOALLOC_SCRATCH_BYTES) return DSA_ERR_WORKSPACE_TOO_SMALL before
+ *     any launch.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the one array: calls whose kernels overlap on a GPU
+ *     (other streams, other threads) race on it and give wrong results; order
+ *     them on one stream.  The array keeps the last call's contents; nothing in
+ *     it needs to start at zero.
+ */
+int dsa_sparse_mla_decode_noalloc(const uint16_t* q, int32_t heads, float sm_scale,
+                                  const dsa_paged_cache* kv, const dsa_rows* rows,
+                                  const int32_t* idx, const int32_t* count, int32_t k,
+                                  int32_t num_splits, float* out, float* out_lse,
+                                  int32_t* d_err, void* stream);
+
+/*
  * dsa_lse_merge -- merge num_parts partial attention results over disjoint
  * token sets (DCP page, Modifications / Sparse decode: partial results are
  * merged by their LSE):  lse = ln sum_p exp(lse_p),
