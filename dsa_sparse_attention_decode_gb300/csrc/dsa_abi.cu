@@ -266,6 +266,7 @@ int dsa_sparse_mla_decode(const uint16_t* q, int32_t heads, float sm_scale,
   const size_t need = dsa_sparse_mla_decode_workspace_size(R, heads, k, num_splits);
   if (workspace_bytes < need || (need > 0 && workspace == nullptr))
     return DSA_ERR_WORKSPACE_TOO_SMALL;
+  if (static_cast<long long>(kv->num_pages) * kv->page_size > INT32_MAX) return DSA_ERR_UNSUPPORTED;
   MlaLaunch L{};
   fill_mla_shard(L, 0, *kv);
   L.page_size = kv->page_size;
@@ -321,6 +322,8 @@ static int check_decode(const dsa_decode_desc* d) {
     if (st != DSA_OK) return st;
     st = check_cache(&d->kv[w], kKvDim);
     if (st != DSA_OK) return st;
+    if (static_cast<long long>(d->kv[w].num_pages) * d->kv[w].page_size > INT32_MAX)
+      return DSA_ERR_UNSUPPORTED;
     if (d->idx_k[w].dtype != d->idx_k[0].dtype || d->kv[w].dtype != d->kv[0].dtype ||
         d->idx_k[w].page_size != d->idx_k[0].page_size ||
         d->kv[w].page_size != d->kv[0].page_size)

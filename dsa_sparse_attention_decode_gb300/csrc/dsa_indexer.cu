@@ -124,7 +124,8 @@ __device__ PairInfo pair_info(const IndexerLaunch& P, int pair, bool report) {
     len = max(len, shard_valid_len(pos, P.W, shard));
   }
   if (static_cast<long long>(len) >
-      static_cast<long long>(P.max_blocks[sl]) * P.page_size) {
+          static_cast<long long>(P.max_blocks[sl]) * P.page_size ||
+      len > P.ld) {
     if (report) raise_err(P.d_err, DSA_DEVERR_POS);
     return pi;
   }
@@ -327,6 +328,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           wk.next(P);
         }
+        // bf16: the stage releases are tcgen05 commits whose arrivals land
+        // asynchronously; the last one of every stage must have landed before
+        // the CTA exits, or it could reach the shared memory of a later CTA
+        if (!kFp8 && !*abort_flag) {
+          for (int s = 0; s < L.stages && s < issued; ++s) {
+            const int last = s + ((issued - 1 - s) / L.stages) * L.stages;
+            mbar_wait(bar(B_KEMPTY + s), static_cast<uint32_t>(last / L.stages) & 1u, abort_flag);
+          }
+        }
         // every issued load must land before the CTA exits (only pending
         // after an abort; otherwise the consumers already waited for them)
         if (*abort_flag) {
@@ -424,30 +434,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       int op = 0;
       uint32_t op_phase = 0;
       int pair_j = -1, last_pair = -1;
+      // A failed (timed-out) wait stops the work of this thread but it keeps
+      // passing the same named barriers as its partner warp.
       bool ok = true;
-      for (int u = 0; u < nunits && ok; ++u) {
+      for (int u = 0; u < nunits; ++u) {
         if (wk.pair != last_pair) {
           ++pair_j;
           last_pair = wk.pair;
           const int mslot = pair_j & 1;
-          if (pair_j >= 2 &&
-              !mbar_wait(bar(B_PEMPTY + mslot), static_cast<uint32_t>((pair_j >> 1) - 1) & 1u,
-                         abort_flag)) {
-            ok = false;
-            break;
-          }
-          if (pair_j >= 1 &&
-              !mbar_wait(bar(B_QEMPTY), static_cast<uint32_t>(pair_j - 1) & 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
+          if (ok && pair_j >= 2)
+            ok = mbar_wait(bar(B_PEMPTY + mslot), static_cast<uint32_t>((pair_j >> 1) - 1) & 1u,
+                           abort_flag);
+          if (ok && pair_j >= 1)
+            ok = mbar_wait(bar(B_QEMPTY), static_cast<uint32_t>(pair_j - 1) & 1u, abort_flag);
           const int sl = wk.pair / P.num_reqs;
           const int shard = P.shard_base + sl;
           const int nr = wk.pi.nr;
           const int row0 = wk.pi.row0;
           PairMeta& m = meta[mslot];
           // one query head-row (128 dims) per thread and step
-          for (int n = at; n < nr * kIdxHeads; n += 64) {
+          for (int n = at; ok && n < nr * kIdxHeads; n += 64) {
             const int g = n / kIdxHeads;
             const int h = n - g * kIdxHeads;
             const uint4* src = reinterpret_cast<const uint4*>(
@@ -499,25 +505,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             m.w[g][h] = wv;
           }
-          if (at < nr) {
+          if (ok && at < nr) {
             const int r = row0 + at;
             m.row[at] = r;
             m.valid[at] = shard_valid_len(__ldg(P.row_pos + r), P.W, shard);
           }
           fence_proxy_async_smem();
           named_bar_sync(1, 64);
-          if (at == 0) {
+          if (ok && at == 0) {
             mbar_arrive(bar(B_QFULL));
             mbar_arrive(bar(B_PFULL + mslot));
           }
         }
         if (kFp8) {
           // convert the raw e4m3 tile into the f16 operand buffer
-          if (!mbar_wait(bar(B_KFULL + stage), phase, abort_flag) ||
-              !mbar_wait(bar(B_OPEMPTY + op), op_phase ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
+          if (ok) ok = mbar_wait(bar(B_KFULL + stage), phase, abort_flag);
+          if (ok) ok = mbar_wait(bar(B_OPEMPTY + op), op_phase ^ 1u, abort_flag);
           const uint8_t* rawp = sbase + L.off_ring + stage * L.stage_bytes;
           uint8_t* opp = sbase + L.off_op + op * kOpBytes;
           const int wi = at >> 5;  // 0..1
@@ -525,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kb = l16 >> 3;
           const int ch = l16 & 7;
 #pragma unroll 4
-          for (int it = 0; it < 32; ++it) {
+          for (int it = 0; ok && it < 32; ++it) {
             const int r = (it * 2 + wi) * 2 + (lane >> 4);
             const uint2 v = *reinterpret_cast<const uint2*>(rawp + r * 128 + l16 * 8);
             const uint4 o = e4m3x8_to_f16x8(v);
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           fence_proxy_async_smem();
           named_bar_sync(1, 64);
-          if (at == 0) {
+          if (ok && at == 0) {
             mbar_arrive(bar(B_KEMPTY + stage));
             mbar_arrive(bar(B_OPFULL + op));
           }
@@ -547,6 +550,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         wk.next(P);
+      }
+      // the operand buffers' last releases are tcgen05 commits whose arrivals
+      // land asynchronously: wait for them before the CTA can exit
+      if (kFp8 && ok && at == 0) {
+        for (int u = max(0, nunits - 2); u < nunits; ++u)
+          mbar_wait(bar(B_OPEMPTY + (u & 1)), static_cast<uint32_t>(u >> 1) & 1u, abort_flag);
       }
     } else {
       // ------------------------------------------------ epilogue (warps 4..7)
