@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--impl", default="product", choices=["product", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--kernel", default=None, choices=["indexer", "topk", "mla"],
+                    help="time one kernel of the step alone on the same workload (a short "
+                         "run for profilers: W warm-up launches, then K timed ones)")
     return ap.parse_args()
 
 
@@ -208,6 +211,65 @@ def algorithmic_bytes(wl):
 
 
 # ----------------------------------------------------------------- product arm
+
+
+def run_kernel_only(args):
+    """One kernel of the step on the benchmark's workload: `warmup` untimed
+    launches, then `steps` timed ones with the L2 flush between them.  The
+    launches a profiler should capture are the last `steps` of that kernel."""
+    import torch
+
+    import dsa_sparse_attention_decode_gb300 as pkg
+    from dsa_sparse_attention_decode_gb300 import api
+    from workloads import config_spec, make_workload
+    from workloads.device import decode_args, upload
+
+    pkg.build()
+    pkg.lib()
+    dev = torch.device("cuda", 0)
+    wl = make_workload(config_spec(1))
+    dw = upload(wl, dev)
+    R, H, k = wl.R, wl.H, wl.topk
+    out = torch.empty(R, H, 512, device=dev)
+    lse = torch.empty(R, H, device=dev)
+    tidx = torch.empty(R, k, dtype=torch.int32, device=dev)
+    tcnt = torch.empty(R, dtype=torch.int32, device=dev)
+    desc = decode_args(dw, False, out, lse, tidx, tcnt)
+    lay = api.dsa_decode_workspace_layout(desc)
+    ws = torch.zeros(lay.total_bytes, dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    api.dsa_decode(desc, ws, err)  # produces the scores and selections the kernels read
+    scores = ws[lay.scores: lay.scores + R * lay.ld_scores * 4].view(torch.float32).view(
+        R, lay.ld_scores)
+    valid = (dw.rows.row_pos + 1).to(torch.int32)
+    mla_ws = torch.empty(max(1, api.dsa_sparse_mla_decode_workspace_size(R, H, k, lay.num_splits)),
+                         dtype=torch.uint8, device=dev)
+    fn = {
+        "indexer": lambda: api.dsa_indexer_scores(dw.q_idx, dw.w_idx, dw.idx_k, dw.rows, scores,
+                                                  err),
+        "topk": lambda: api.dsa_topk(scores, valid, k, tidx, tcnt, err),
+        "mla": lambda: api.dsa_sparse_mla_decode(dw.q, wl.sm_scale, dw.kv, dw.rows, tidx, tcnt,
+                                                 out, lse, err, workspace=mla_ws,
+                                                 num_splits=lay.num_splits),
+    }[args.kernel]
+    flush_w = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    ms = []
+    for i in range(args.warmup + args.steps):
+        flush_w.zero_()
+        flush_r.sum()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            ms.append(a.elapsed_time(b))
+    if api.dsa_read_error(err) != 0:
+        raise SystemExit("device error word set")
+    print(json.dumps({"kernel": args.kernel, "workload": WORKLOAD, "launches": args.steps,
+                      "us_mean": round(1e3 * float(np.mean(ms)), 2)}), flush=True)
 
 
 def run_product(args):
@@ -428,6 +490,9 @@ def run_reference(args):
 
 if __name__ == "__main__":
     a = parse()
+    if a.kernel is not None:
+        run_kernel_only(a)
+        sys.exit(0)
     if a.warmup < 3 and a.impl == "product":
         a.warmup = 3
     if a.impl == "reference":
