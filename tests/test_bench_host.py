@@ -1,0 +1,61 @@
+"""Host logic of bench.py on CPU: the whole-job aggregation over ranks (gloo,
+world size 2) and the single-process path."""
+
+from __future__ import annotations
+
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, rows, secs, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        value, sec, total = bench.aggregate(rows[rank], secs[rank])
+        out[rank] = torch.tensor([value, sec, total], dtype=torch.float64)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_aggregate_single_process():
+    value, sec, total = bench.aggregate(64.0, 0.5)
+    assert (value, sec, total) == (128.0, 0.5, 64.0)
+
+
+@pytest.mark.timeout(120)
+def test_aggregate_over_two_gloo_ranks():
+    """value = rows of all ranks / the slowest rank's time, on every rank."""
+    world = 2
+    rows = [32.0, 32.0]
+    secs = [0.25, 0.40]
+    out = torch.zeros(world, 3, dtype=torch.float64).share_memory_()
+    mp.spawn(_rank_main, args=(world, _free_port(), rows, secs, out), nprocs=world, join=True)
+    for r in range(world):
+        value, sec, total = out[r].tolist()
+        assert total == 64.0
+        assert sec == 0.40
+        assert value == pytest.approx(64.0 / 0.40)
+
+
+def test_kernel_mode_is_parsed(monkeypatch):
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--kernel", "topk", "--steps", "2", "--warmup", "1"])
+    a = bench.parse()
+    assert a.kernel == "topk" and a.steps == 2 and a.warmup == 1 and a.gpus == 1
