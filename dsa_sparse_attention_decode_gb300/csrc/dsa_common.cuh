@@ -169,6 +169,41 @@ DSA_DEV bool named_bar_or(int id, int nthreads, bool pred) {
   return out != 0;
 }
 
+// ----------------------------------------------------------------- clusters
+
+DSA_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster; orders shared-memory writes before
+// the barrier with reads (also remote ones) after it
+DSA_DEV void cluster_sync() {
+  __syncwarp();  // the .aligned forms need a converged warp
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// the shared-memory address `saddr` of this CTA, mapped into CTA `rank`
+DSA_DEV uint32_t dsmem_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+DSA_DEV uint4 dsmem_ld_v4(uint32_t caddr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(caddr)
+               : "memory");
+  return v;
+}
+DSA_DEV uint32_t dsmem_ld(uint32_t caddr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+  return v;
+}
+
 // ----------------------------------------------------------------- tcgen05
 //
 // Every helper below whose instruction is warp-collective (.sync.aligned, and

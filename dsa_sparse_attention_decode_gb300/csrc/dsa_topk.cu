@@ -4,18 +4,20 @@
 // Motivation: DSA keeps the top 2048 tokens of the whole sequence; Modifications
 // / Indexer decode: every shard first keeps a local top-k of its own tokens.
 //
-// One CTA of 1024 threads per score row:
-//   1. scores become order-preserving uint32 keys (-0 == +0), cached in shared
-//      memory when the row fits; the same pass builds a histogram of the top
-//      13 key bits;
-//   2. the bin holding the k-th largest key is refined with two more
-//      histograms (10 and 9 bits) over only the keys still in play, giving the
-//      exact threshold key T and how many keys equal to T are taken (the
-//      lowest positions win ties);
+// One cluster of kCluster CTAs (1024 threads each) per score row; CTA c owns
+// the c-th contiguous segment of the row:
+//   1. its scores become order-preserving uint32 keys (-0 == +0), cached in
+//      shared memory when the segment fits; the same pass builds the segment's
+//      histogram of the top 13 key bits;
+//   2. every CTA sums the cluster's histograms through distributed shared
+//      memory and finds the bin holding the k-th largest key; two more
+//      histograms (10 and 9 bits) over only the keys still in play refine it
+//      to the exact threshold key T and how many keys equal to T are taken
+//      (the lowest positions win ties);
 //   3. an order-preserving compaction writes the selected positions in
-//      ascending order: every warp owns a contiguous segment of the row,
-//      counts its keys above / equal to T, and after one exclusive scan over
-//      the warps writes its selected positions at their final slots.
+//      ascending order: each CTA learns from the others' counts where its
+//      segment's selections start, then every warp owns a contiguous piece of
+//      the segment and writes its selected positions at their final slots.
 // No sort: the list comes out in position order.
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
@@ -26,41 +28,70 @@ namespace {
 
 constexpr int kThreads = kSelThreads;
 constexpr int kWarps = kThreads / 32;
+constexpr int kCluster = 4;  // CTAs per score row
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kBins1 = kSelBins1;
 constexpr int kShift1 = kSelShift1;
 
 struct TopkSmem {
-  int cap;         // keys cached in smem
-  int off_keys, off_hist, off_misc, total;
+  int cap;         // keys of the CTA's segment cached in smem
+  int off_hist, off_red, off_misc, off_keys, total;
 };
 
 __host__ inline TopkSmem topk_smem() {
   TopkSmem s{};
-  s.off_hist = 0;
-  s.off_misc = s.off_hist + kBins1 * 4;
+  s.off_hist = 0;                       // this CTA's histogram (read by the cluster)
+  s.off_red = s.off_hist + kBins1 * 4;  // the cluster's summed histogram
+  s.off_misc = s.off_red + kBins1 * 4;
   s.off_keys = s.off_misc + 1024;
   s.cap = ((kSmemLimit - s.off_keys) / 4) & ~1023;
   s.total = s.off_keys + s.cap * 4;
   return s;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// red[b] = sum over the cluster's CTAs of hist[b], b < nb (nb a multiple of
+// 4 * kThreads or smaller than it, and of 4)
+__device__ __forceinline__ void cluster_sum_hist(const uint32_t* hist, uint32_t* red, int nb) {
+  const uint32_t base = smem_u32(hist);
+  for (int v = threadIdx.x; v < nb / 4; v += kThreads) {
+    uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int c = 0; c < kCluster; ++c) {
+      const uint4 x = dsmem_ld_v4(dsmem_map(base + v * 16, c));
+      acc.x += x.x;
+      acc.y += x.y;
+      acc.z += x.z;
+      acc.w += x.w;
+    }
+    reinterpret_cast<uint4*>(red)[v] = acc;
+  }
+  __syncthreads();
+}
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     topk_kernel(const TopkLaunch P, const TopkSmem S) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + S.off_hist);
+  uint32_t* red = reinterpret_cast<uint32_t*>(smem + S.off_red);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + S.off_misc);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + S.off_keys);
   uint32_t* scratch = misc;       // 32 words
   uint32_t* sh = misc + 64;       // shared scalars
+  uint32_t* cnt = misc + 96;      // [2] this CTA's keys above / equal to T (read by the cluster)
+  uint32_t* wgt = misc + 128;     // [32] keys above T per warp
+  uint32_t* weq = misc + 160;     // [32] keys equal to T per warp
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const int q = blockIdx.x;
+  const int warp = tid >> 5;
+  const uint32_t crank = cluster_ctarank();
+  const int q = blockIdx.x / kCluster;
   const int w = q / P.rows;
   const int r = q - w * P.rows;
   const int k = P.k;
 
+  // every CTA of the cluster derives the same n, so all take the same branches
+  // and pass the same cluster barriers
   int n;
   if (P.valid_len) {
     n = P.valid_len[q];
@@ -68,25 +99,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     n = shard_valid_len(P.row_pos[r], P.W, w + P.shard_offset);
   }
   if (n < 0 || n > P.ld) {
-    if (tid == 0) raise_err(P.d_err, DSA_DEVERR_INDEX);
+    if (tid == 0 && crank == 0) raise_err(P.d_err, DSA_DEVERR_INDEX);
     n = n < 0 ? 0 : static_cast<int>(P.ld);
   }
   const float* src = P.scores + static_cast<long long>(w) * P.shard_stride +
                      static_cast<long long>(r) * P.ld;
-  const bool in_smem = n <= S.cap;
+  // this CTA's segment [c0, c1) of the row, 32-aligned starts
+  const int cseg = (((n + kCluster - 1) / kCluster) + 31) & ~31;
+  const int c0 = min(n, static_cast<int>(crank) * cseg);
+  const int c1 = min(n, c0 + cseg);
+  const int m = c1 - c0;
+  const bool in_smem = m <= S.cap;
   const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
-  const int cnt = n < k ? n : k;
+  const int cnt_all = n < k ? n : k;
+  const bool need_select = n > k;
 
   for (int b = tid; b < kBins1; b += kThreads) hist[b] = 0;
   if (tid < 16) sh[tid] = 0;
   __syncthreads();
 
   // ---------------- pass 1: keys (+ smem copy) and the 13-bit histogram
-  const bool need_select = n > k;
   bool nan_seen = false;
   {
-    const int nv = vec ? (n >> 2) : 0;
-    const float4* src4 = reinterpret_cast<const float4*>(src);
+    const float* seg = src + c0;
+    const int nv = vec ? (m >> 2) : 0;
+    const float4* src4 = reinterpret_cast<const float4*>(seg);
     for (int base = 0; base < nv; base += kThreads * 4) {
       float4 v[4];
 #pragma unroll
@@ -111,8 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    for (int i = nv * 4 + tid; i < n; i += kThreads) {
-      const float f = __ldg(src + i);
+    for (int i = nv * 4 + tid; i < m; i += kThreads) {
+      const float f = __ldg(seg + i);
       nan_seen |= (f != f);
       const uint32_t key = score_key(f);
       if (need_select) atomicAdd(hist + (key >> kShift1), 1u);
@@ -123,30 +160,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (tid == 0 && sh[0]) raise_err(P.d_err, DSA_DEVERR_NAN);
 
+  // key of row position i of this CTA's segment
   auto key_at = [&](int i) -> uint32_t {
-    return in_smem ? keys[i] : score_key(__ldg(src + i));
+    return in_smem ? keys[i - c0] : score_key(__ldg(src + i));
   };
 
+  uint32_t T = 0, k_rem = 0;
+  if (need_select) {
+    // ---------------- the exact k-th largest key over the cluster's histograms
+    cluster_sync();                       // every CTA's 13-bit histogram is complete
+    cluster_sum_hist(hist, red, kBins1);
+    find_bin(red, kBins1, static_cast<uint32_t>(k), scratch, sh + 4);
+    const uint32_t b1 = sh[4];
+    k_rem = sh[5];
+    cluster_sync();                       // every CTA has read the histograms
+    for (int b = tid; b < kSelBins2; b += kThreads) hist[b] = 0;
+    __syncthreads();
+    for (int i = c0 + tid; i < c1; i += kThreads) {
+      const uint32_t key = key_at(i);
+      if ((key >> kShift1) == b1) atomicAdd(hist + ((key >> kSelShift2) & (kSelBins2 - 1)), 1u);
+    }
+    cluster_sync();
+    cluster_sum_hist(hist, red, kSelBins2);
+    find_bin(red, kSelBins2, k_rem, scratch, sh + 4);
+    const uint32_t pre2 = (b1 << (kShift1 - kSelShift2)) | sh[4];
+    k_rem = sh[5];
+    cluster_sync();
+    for (int b = tid; b < kSelBins3; b += kThreads) hist[b] = 0;
+    __syncthreads();
+    for (int i = c0 + tid; i < c1; i += kThreads) {
+      const uint32_t key = key_at(i);
+      if ((key >> kSelShift2) == pre2) atomicAdd(hist + (key & (kSelBins3 - 1)), 1u);
+    }
+    cluster_sync();
+    cluster_sum_hist(hist, red, kSelBins3);
+    find_bin(red, kSelBins3, k_rem, scratch, sh + 4);
+    T = (pre2 << kSelShift2) | sh[4];
+    k_rem = sh[5];  // keys equal to T that are taken (the lowest positions)
+  }
+
+  // ---------------- order-preserving compaction
   const int off = P.index_offset + (P.offset_per_shard ? (w + P.shard_offset) : 0);
   int32_t* oi = P.out_idx + static_cast<long long>(q) * k;
   float* os = P.out_score ? P.out_score + static_cast<long long>(q) * k : nullptr;
-
-  uint32_t T = 0, k_rem = 0;
-  bool all = true;  // n <= k: every position is selected
-  if (need_select) {
-    all = false;
-    // ---------------- refine the threshold bin to the exact k-th key
-    refine_threshold(key_at, [](int) { return true; }, n, static_cast<uint32_t>(k), hist,
-                     scratch, sh + 4, T, k_rem);
-    // k_rem: keys equal to T that are taken (the lowest positions)
-  }
-
-  // ---------------- order-preserving compaction by warp segments
-  const int warp = tid >> 5;
-  const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
-  const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
-  uint32_t* wgt = misc + 128;  // [32] keys above T per warp
-  uint32_t* weq = misc + 160;  // [32] keys equal to T per warp
+  const bool all = !need_select;  // n <= k: every position is selected
+  const int wseg = ((m + kWarps - 1) / kWarps + 31) & ~31;
+  const int s0 = min(c1, c0 + warp * wseg), s1 = min(c1, s0 + wseg);
   {
     uint32_t cg = 0, ce = 0;
     if (!all) {
@@ -165,7 +224,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
+  if (tid == 0) {
+    uint32_t g = 0, e = 0;
+    for (int v = 0; v < kWarps; ++v) {
+      g += wgt[v];
+      e += weq[v];
+    }
+    cnt[0] = g;
+    cnt[1] = e;
+  }
+  cluster_sync();  // every CTA's counts are visible to the cluster
+  // selections and ties of the segments before this one (lower positions)
   uint32_t eq_before = 0, sel_before = 0;
+  for (uint32_t c = 0; c < crank; ++c) {
+    const uint32_t g = dsmem_ld(dsmem_map(smem_u32(cnt), c));
+    const uint32_t e = dsmem_ld(dsmem_map(smem_u32(cnt + 1), c));
+    const uint32_t take = eq_before >= k_rem ? 0u : min(e, k_rem - eq_before);
+    sel_before += g + take;
+    eq_before += e;
+  }
   for (int v = 0; v < warp; ++v) {
     const uint32_t e = weq[v];
     const uint32_t take = eq_before >= k_rem ? 0u : min(e, k_rem - eq_before);
@@ -190,11 +267,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     eq_before += __popc(me);
     sel_before += __popc(ms);
   }
-  for (int i = cnt + tid; i < k; i += kThreads) {
-    oi[i] = -1;
-    if (os) os[i] = -__int_as_float(0x7f800000);
+  if (crank == 0) {
+    for (int i = cnt_all + tid; i < k; i += kThreads) {
+      oi[i] = -1;
+      if (os) os[i] = -__int_as_float(0x7f800000);
+    }
+    if (tid == 0) P.out_count[q] = cnt_all;
   }
-  if (tid == 0) P.out_count[q] = cnt;
+  cluster_sync();  // no CTA leaves while another may still read its counts
 }
 
 }  // namespace
@@ -204,9 +284,9 @@ cudaError_t launch_topk(const TopkLaunch& p, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S.total);
   if (e != cudaSuccess) return e;
-  const int grid = p.nshards * p.rows;
-  if (grid == 0) return cudaSuccess;
-  topk_kernel<<<grid, kThreads, S.total, stream>>>(p, S);
+  const int rows = p.nshards * p.rows;
+  if (rows == 0) return cudaSuccess;
+  topk_kernel<<<rows * kCluster, kThreads, S.total, stream>>>(p, S);
   return cudaGetLastError();
 }
 
