@@ -7,11 +7,13 @@
 // with a single split the partial is the final result and goes straight to
 // the caller's output.
 //
-// One CTA (8 warps) per (work row, split).  The split's selected positions are
-// resolved through the block table once; then 64-token tiles of 576-wide
-// latent rows are gathered with 16-byte cp.async into a double buffer (fp8
-// rows are widened to f16 in shared memory: e4m3 values are f16 values) and
-// every head of the row shares each gathered tile:
+// One CTA per (work row, split), 10 warps.  The split's selected positions are
+// resolved through the block table once.  Warps 8-9 then gather 64-token tiles
+// of 576-wide latent rows with 16-byte cp.async into a double buffer (each
+// thread's copies arrive on the tile's mbarrier as they land), so the gather
+// runs while warps 0-7 compute on the previous tile; fp8 rows land raw and are
+// widened to f16 by the compute warps (e4m3 values are f16 values).  Every head
+// of the row shares each gathered tile:
 //   S = q . kv^T (all 576 dims), online softmax in fp32 (base 2), P split into
 //   two bf16 parts (f16 for fp8 rows), O += P . v (first 512 dims).
 // The fp8 path multiplies each logit by the token's scale and folds the scale
@@ -27,7 +29,9 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kCompute = 256;                 // warps 0..7: tensor-core math
+constexpr int kGather = 64;                   // warps 8..9: the row gather
+constexpr int kThreads = kCompute + kGather;
 constexpr int kTile = 64;                 // tokens per tile
 constexpr int kRowB = kKvDim * 2 + 16;    // padded smem row of 576 16-bit values
 constexpr int kPRowB = kTile * 2 + 16;    // padded smem row of P
@@ -35,7 +39,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct MlaSmem {
-  int off_q, off_kv, off_raw, off_p, off_red, off_rowoff, off_kscale, off_misc, total;
+  int off_q, off_kv, off_raw, off_p, off_red, off_rowoff, off_kscale, off_misc, off_bar, total;
   int kv_bufs;
 };
 
@@ -59,18 +63,13 @@ __host__ __device__ inline MlaSmem mla_smem(int heads, int fp8, int chunk) {
   off += fp8 ? chunk * 4 : 0;
   s.off_misc = off;
   off += 64 * 4 + heads * 4;
+  off = (off + 15) & ~15;
+  s.off_bar = off;  // mbarriers: full[2], empty[2], abort flag
+  off += 64;
   s.total = off;
   return s;
 }
 
-DSA_DEV void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-DSA_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-DSA_DEV void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 DSA_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -133,6 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
   long long* rowoff = reinterpret_cast<long long*>(smem + S.off_rowoff);
   float* kscale_s = reinterpret_cast<float*>(smem + S.off_kscale);
   int* misc = reinterpret_cast<int*>(smem + S.off_misc);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S.off_bar);  // full[2], empty[2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4);
   float* qexp = reinterpret_cast<float*>(smem + S.off_misc + 64 * 4);  // [H] logit scales
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -180,6 +181,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
       b = -1;
     }
     misc[0] = b;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(bars + i), kGather);   // tile landed: every gather thread's copies
+      mbar_init(smem_u32(bars + 2 + i), 1);     // buffer free: one compute thread
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
   }
 
   // query -> smem (bf16 copy; fp8 path: f16 with a per-head power of two)
@@ -190,10 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
       cp_async16(smem_u32(q_s + h * kRowB + cc * 16), qsrc + h * kKvDim + cc * 8);
     }
     cp_async_commit();
+    cp_async_wait<0>();
     if (tid < H) qexp[tid] = P.sm_scale * kLog2e;
   } else {
     // one warp per head: max |q| -> exponent -> scaled f16 copy
-    for (int h = warp; h < H; h += 8) {
+    for (int h = warp; h < H; h += kThreads / 32) {
       const uint16_t* src = qsrc + h * kKvDim;
       uint32_t mx = 0;
       for (int i = lane; i < kKvDim; i += 32) mx = max(mx, static_cast<uint32_t>(src[i] & 0x7FFFu));
@@ -242,34 +250,45 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
   const uint8_t* kvbase = static_cast<const uint8_t*>(P.kv[w]);
   const int ntiles = (ntok + kTile - 1) / kTile;
 
-  auto issue_gather = [&](int tile, int buf) {
-    const int t0 = tile * kTile;
-    if (!kFp8) {
-      uint8_t* dst = kv_s + buf * kTile * kRowB;
-      for (int c = tid; c < kTile * 72; c += kThreads) {
-        const int row = c / 72, cc = c - row * 72;
-        const long long off = (t0 + row < ntok) ? rowoff[t0 + row] : -1;
-        if (off >= 0) {
-          cp_async16(smem_u32(dst + row * kRowB + cc * 16), kvbase + off * (kKvDim * 2) + cc * 16);
-        } else {
-          *reinterpret_cast<uint4*>(dst + row * kRowB + cc * 16) = make_uint4(0, 0, 0, 0);
-        }
+  if (warp >= kCompute / 32) {
+    // ================================================= row gather (warps 8, 9)
+    // Tile i goes to buffer i & 1 once the compute warps have released it.
+    // Each of the 64 threads moves one selected latent row with one bulk copy
+    // (the copy engine takes whole rows; scattered 16-byte copies were bound
+    // by their issue rate) and arrives on the tile's barrier with the bytes it
+    // expects; a row past the split is zero-filled before the arrival.
+    const int gt = tid - kCompute;  // the tile row this thread moves
+    constexpr uint32_t kRowBytes = kFp8 ? kKvDim : kKvDim * 2;
+    int issued = 0;
+    for (int tile = 0; tile < ntiles; ++tile) {
+      const int buf = tile & 1, use = tile >> 1;
+      if (use >= 1 &&
+          !mbar_wait(smem_u32(bars + 2 + buf), static_cast<uint32_t>(use - 1) & 1u, abort_flag))
+        break;
+      const int t0 = tile * kTile;
+      const uint32_t full = smem_u32(bars + buf);
+      uint8_t* dst = kFp8 ? raw_s + buf * kTile * kKvDim + gt * kKvDim
+                          : kv_s + buf * kTile * kRowB + gt * kRowB;
+      const long long off = (t0 + gt < ntok) ? rowoff[t0 + gt] : -1;
+      if (off >= 0) {
+        mbar_arrive_expect_tx(full, kRowBytes);
+        bulk_copy_g2s(smem_u32(dst), kvbase + off * kRowBytes, kRowBytes, full);
+      } else {
+        for (uint32_t c = 0; c < kRowBytes; c += 16)
+          *reinterpret_cast<uint4*>(dst + c) = make_uint4(0u, 0u, 0u, 0u);
+        mbar_arrive(full);
       }
-    } else {
-      uint8_t* dst = raw_s + buf * kTile * kKvDim;
-      for (int c = tid; c < kTile * 36; c += kThreads) {
-        const int row = c / 36, cc = c - row * 36;
-        const long long off = (t0 + row < ntok) ? rowoff[t0 + row] : -1;
-        if (off >= 0) {
-          cp_async16(smem_u32(dst + row * kKvDim + cc * 16), kvbase + off * kKvDim + cc * 16);
-        } else {
-          *reinterpret_cast<uint4*>(dst + row * kKvDim + cc * 16) = make_uint4(0, 0, 0, 0);
-        }
-      }
+      ++issued;
     }
-    cp_async_commit();
-  };
-
+    // after an abort the compute warps stop waiting: every copy still in
+    // flight must land before the CTA exits
+    if (*abort_flag) {
+      volatile int no_abort = 0;
+      for (int tile = max(0, issued - 2); tile < issued; ++tile)
+        mbar_wait(smem_u32(bars + (tile & 1)), static_cast<uint32_t>(tile >> 1) & 1u, &no_abort);
+    }
+  } else {
+  // ================================================= compute (warps 0..7)
   // per-thread state: O accumulators for dims [64*warp, 64*warp+64) of all heads
   float o[MT][8][4];
 #pragma unroll
@@ -289,20 +308,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
   const float qsc0 = qexp[mt_s * 16 + g];
   const float qsc1 = qexp[mt_s * 16 + g + 8];
 
-  issue_gather(0, 0);
   for (int tile = 0; tile < ntiles; ++tile) {
-    const int buf = kFp8 ? 0 : (tile & 1);
-    if (tile + 1 < ntiles) {
-      issue_gather(tile + 1, kFp8 ? ((tile + 1) & 1) : ((tile + 1) & 1));
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
+    const int fb = tile & 1;  // the gathered tile's buffer (raw rows for fp8)
+    // a timed-out wait (abort flag set) computes on whatever is there; the
+    // error word reports it and every barrier below is still passed
+    mbar_wait(smem_u32(bars + fb), static_cast<uint32_t>(tile >> 1) & 1u, abort_flag);
+    const int buf = kFp8 ? 0 : fb;
     uint8_t* kv = kv_s + buf * kTile * kRowB;
     if (kFp8) {
-      const uint8_t* rawp = raw_s + (tile & 1) * kTile * kKvDim;
-      for (int c = tid; c < kTile * 72; c += kThreads) {
+      const uint8_t* rawp = raw_s + fb * kTile * kKvDim;
+      for (int c = tid; c < kTile * 72; c += kCompute) {
         const int row = c / 72, cc = c - row * 72;
         const uint2 v = *reinterpret_cast<const uint2*>(rawp + row * kKvDim + cc * 8);
         uint4 out;
@@ -317,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
         out.w = h.x | (static_cast<uint32_t>(h.y) << 16);
         *reinterpret_cast<uint4*>(kv + row * kRowB + cc * 16) = out;
       }
-      __syncthreads();
+      named_bar_sync(1, kCompute);
+      if (tid == 0) mbar_arrive(smem_u32(bars + 2 + fb));  // the raw buffer is free
     }
     const int t0 = tile * kTile;
     const uint32_t kv_a = smem_u32(kv);
@@ -373,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
       red[tg * H + mt_s * 16 + g] = mx0;
       red[tg * H + mt_s * 16 + g + 8] = mx1;
     }
-    __syncthreads();
+    named_bar_sync(1, kCompute);
     // new running max for every head row this thread touches
     float alpha[MT][2];
 #pragma unroll
@@ -426,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
       l_part[0] = l_part[0] * alpha[mt_s][0] + ls0;
       l_part[1] = l_part[1] * alpha[mt_s][1] + ls1;
     }
-    __syncthreads();
+    named_bar_sync(1, kCompute);
 
     // ---- O += P . v for value dims [64*warp, 64*warp + 64)
 #pragma unroll
@@ -470,7 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
         }
       }
     }
-    __syncthreads();
+    named_bar_sync(1, kCompute);
+    if (!kFp8 && tid == 0) mbar_arrive(smem_u32(bars + 2 + fb));  // the tile's buffer is free
   }
 
   // ---- softmax denominators: sum the row partials over t4 and token groups
@@ -484,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
     red2[tg * H + mt_s * 16 + g] = l0;
     red2[tg * H + mt_s * 16 + g + 8] = l1;
   }
-  __syncthreads();
+  named_bar_sync(1, kCompute);
   const int d0 = warp * 64;
 #pragma unroll
   for (int a = 0; a < MT; ++a) {
@@ -505,6 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
       }
     }
   }
+  }
+
+  __syncthreads();
+  if (tid == 0 && *abort_flag) raise_err(P.d_err, DSA_DEVERR_TIMEOUT);
 }
 
 template <int H, bool F>
