@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--impl", default="product", choices=["product", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--config", type=int, default=None,
+                    help="time the fused step on configuration 0..4 instead (device time only, "
+                         "one JSON line; the contract line is the default configuration 1)")
+    ap.add_argument("--batch", type=int, default=None, help="requests of configuration 4")
     ap.add_argument("--kernel", default=None, choices=["indexer", "topk", "mla"],
                     help="time one kernel of the step alone on the same workload (a short "
                          "run for profilers: W warm-up launches, then K timed ones)")
@@ -213,6 +217,57 @@ def algorithmic_bytes(wl):
 # ----------------------------------------------------------------- product arm
 
 
+def run_config(args):
+    """The fused step on another configuration: `warmup` untimed steps, then
+    `steps` timed ones (CUDA events, L2 flushed before each)."""
+    import torch
+
+    import dsa_sparse_attention_decode_gb300 as pkg
+    from dsa_sparse_attention_decode_gb300 import api
+    from workloads import config_spec, make_workload
+    from workloads.device import decode_args, upload
+
+    pkg.build()
+    pkg.lib()
+    dev = torch.device("cuda", 0)
+    kw = {"B": args.batch} if (args.config == 4 and args.batch) else {}
+    spec = config_spec(args.config, **kw)
+    wl = make_workload(spec)
+    dw = upload(wl, dev, shards=spec.shards > 1, unsharded=spec.shards == 1)
+    R, H, k = wl.R, wl.H, wl.topk
+    out = torch.empty(R, H, 512, device=dev)
+    lse = torch.empty(R, H, device=dev)
+    desc = decode_args(dw, spec.shards > 1, out, lse)
+    ws = torch.zeros(max(1, api.dsa_decode_workspace_size(desc)), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush_w = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    ms = []
+    for i in range(args.warmup + args.steps):
+        flush_w.zero_()
+        flush_r.sum()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        api.dsa_decode(desc, ws, err)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            ms.append(a.elapsed_time(b))
+    if api.dsa_read_error(err) != 0:
+        raise SystemExit("device error word set")
+    sec = float(np.mean(ms)) / 1e3
+    idx_b, mla_b = algorithmic_bytes(wl)
+    peaks, kind = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    gbs = (idx_b + mla_b) / sec / 1e9
+    print(json.dumps({"config": spec.name, "rows": R, "shards": spec.shards,
+                      "ms_per_step": round(sec * 1e3, 4), "rows_per_s": round(R / sec, 1),
+                      "algorithmic_bytes": idx_b + mla_b, "path_gbs": round(gbs, 1),
+                      "path_frac_of_measured": round(gbs / hbm, 4), "peak_source": kind}),
+          flush=True)
+
+
 def run_kernel_only(args):
     """One kernel of the step on the benchmark's workload: `warmup` untimed
     launches, then `steps` timed ones with the L2 flush between them.  The
@@ -227,7 +282,12 @@ def run_kernel_only(args):
     pkg.build()
     pkg.lib()
     dev = torch.device("cuda", 0)
-    wl = make_workload(config_spec(1))
+    cfg = 1 if args.config is None else args.config
+    kw = {"B": args.batch} if (cfg == 4 and args.batch) else {}
+    spec = config_spec(cfg, **kw)
+    if spec.shards > 1:
+        raise SystemExit("--kernel times the unsharded path; configuration 3 is sharded")
+    wl = make_workload(spec)
     dw = upload(wl, dev)
     R, H, k = wl.R, wl.H, wl.topk
     out = torch.empty(R, H, 512, device=dev)
@@ -268,7 +328,7 @@ def run_kernel_only(args):
             ms.append(a.elapsed_time(b))
     if api.dsa_read_error(err) != 0:
         raise SystemExit("device error word set")
-    print(json.dumps({"kernel": args.kernel, "workload": WORKLOAD, "launches": args.steps,
+    print(json.dumps({"kernel": args.kernel, "workload": spec.name, "launches": args.steps,
                       "us_mean": round(1e3 * float(np.mean(ms)), 2)}), flush=True)
 
 
@@ -492,6 +552,9 @@ if __name__ == "__main__":
     a = parse()
     if a.kernel is not None:
         run_kernel_only(a)
+        sys.exit(0)
+    if a.config is not None:
+        run_config(a)
         sys.exit(0)
     if a.warmup < 3 and a.impl == "product":
         a.warmup = 3

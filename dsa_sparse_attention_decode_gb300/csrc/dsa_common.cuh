@@ -72,19 +72,6 @@ DSA_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of the phase with the given parity (never suspends the
-// thread, unlike try_wait): for loops that poll several barriers.
-DSA_DEV bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 
 // Wait for the phase with the given parity to complete.  Returns false when
 // the CTA-wide abort flag is set or the wait runs past kWaitTimeoutNs (it then
@@ -104,11 +91,6 @@ DSA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) 
   }
 }
 
-// mbar_wait taken by a whole warp: true only if every lane's wait succeeded,
-// so that warp-collective instructions after it stay warp-uniform.
-DSA_DEV bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag)) != 0;
-}
 
 // ----------------------------------------------------------------- TMA
 
@@ -136,14 +118,6 @@ DSA_DEV void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32
       : "memory");
 }
 
-DSA_DEV void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
-                         int c2, int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-      : "memory");
-}
 
 DSA_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -154,20 +128,6 @@ DSA_DEV void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// named barrier that also returns the OR of `pred` over the participating threads
-DSA_DEV bool named_bar_or(int id, int nthreads, bool pred) {
-  __syncwarp();  // the .aligned form needs a converged warp
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}\n"
-      : "=r"(out)
-      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
-      : "memory");
-  return out != 0;
-}
 
 // ----------------------------------------------------------------- clusters
 
@@ -206,10 +166,11 @@ DSA_DEV uint32_t dsmem_ld(uint32_t caddr) {
 
 // ----------------------------------------------------------------- tcgen05
 //
-// Every helper below whose instruction is warp-collective (.sync.aligned, and
-// the bar.sync / bar.red named barriers above) first reconverges the warp with
-// __syncwarp(): those forms are undefined when the warp arrives diverged, and
-// the compiler does not know that an inline-asm instruction needs it.
+// Every helper below whose instruction is warp-collective (.sync.aligned, like
+// the bar.sync named barrier and the cluster barrier above) first reconverges
+// the warp with __syncwarp(): those forms are undefined when the warp arrives
+// diverged, and the compiler does not know that an inline-asm instruction
+// needs it.
 
 DSA_DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   __syncwarp();  // the .aligned form needs a converged warp
@@ -254,65 +215,14 @@ DSA_DEV void tc_commit(uint32_t bar) {
       : "memory");
 }
 
-DSA_DEV void tmem_wait_ld() { __syncwarp(); asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-DSA_DEV void tmem_wait_st() { __syncwarp(); asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// 16 consecutive 32-bit columns of this thread's TMEM lane
-DSA_DEV void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {
+DSA_DEV void tmem_wait_ld() {
   __syncwarp();  // the .aligned form needs a converged warp
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-DSA_DEV void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t* r) {
-  __syncwarp();  // the .aligned form needs a converged warp
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
-DSA_DEV void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t* r) {
-  __syncwarp();  // the .aligned form needs a converged warp
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // cp.async 16 bytes global -> shared (L2 only)
 DSA_DEV void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-// 16 bytes of zeros to shared memory through the same cp.async path (src-size 0)
-DSA_DEV void cp_async16_zero(uint32_t dst, const void* any_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(dst), "l"(any_src)
-               : "memory");
-}
-// arrive on the mbarrier once all prior cp.async of this thread have landed
-// (the barrier's expected count covers these arrivals)
-DSA_DEV void cp_async_mbar_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-// 2^x with the hardware approximation (relative error ~2^-22)
-DSA_DEV float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 DSA_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -341,38 +251,21 @@ DSA_DEV void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
 // Shared-memory matrix descriptor of a K-major operand tile stored with the
 // 128-byte swizzle: rows of 128 bytes, 8-row atoms of 1024 bytes stacked along
 // M/N (stride byte offset 1024); the atom must be 1024-byte aligned.
-DSA_DEV uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo = 1024u) {
+DSA_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
   d |= static_cast<uint64_t>(1u) << 16;                 // leading byte offset (unused)
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;  // bytes between 8-row groups
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;         // stride byte offset
   d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version
   d |= static_cast<uint64_t>(2u) << 61;                 // 128-byte swizzle
   return d;
 }
 
-// Shared-memory matrix descriptor of an MN-major operand stored with the
-// 128-byte swizzle: each 128-byte row holds 64 consecutive M (or N) elements
-// of one K index; 8 K-rows form a 1024-byte atom.  lbo = bytes between the
-// 64-element groups along M/N, sbo = bytes between 8-row groups along K.
-DSA_DEV uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;
-  d |= static_cast<uint64_t>(2u) << 61;
-  return d;
-}
-
-// Instruction descriptor, kind::f16: f32 accumulator.  a_bf16/b_bf16 select
-// bf16 (1) or f16 (0) inputs; a_mn/b_mn select an MN-major (1) or K-major (0)
-// operand.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_bf16, int b_bf16,
-                                                 int a_mn = 0, int b_mn = 0) {
+// Instruction descriptor, kind::f16: f32 accumulator, K-major operands;
+// a_bf16/b_bf16 select bf16 (1) or f16 (0) inputs.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_bf16, int b_bf16) {
   return (1u << 4) | (static_cast<uint32_t>(a_bf16) << 7) |
-         (static_cast<uint32_t>(b_bf16) << 10) | (static_cast<uint32_t>(a_mn) << 15) |
-         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(b_bf16) << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 

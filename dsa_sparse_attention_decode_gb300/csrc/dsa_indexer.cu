@@ -32,6 +32,8 @@ constexpr int kTileT = 128;
 constexpr int kThreads = 256;
 constexpr int kOpBytes = kTileT * kIdxDim * 2;     // 32 KB f16/bf16 operand tile
 constexpr int kRawFp8Bytes = kTileT * kIdxDim;     // 16 KB e4m3 tile
+constexpr int kScaleBytes = kTileT * 4;            // the tile's fp32 token scales
+constexpr int kScaleRing = 8;                      // fp8: tiles of scales kept for the epilogue
 constexpr int kHalfBf16Box = 64 * 64 * 2;          // one TMA box: 64 tokens x 64 dims
 constexpr int kSmemLimit = 227 * 1024;
 
@@ -47,7 +49,7 @@ struct Layout {
   int stage_bytes;
   int q_rows;      // max_rows * 64
   int q_kb_stride; // bytes between the two 64-dim halves of Q
-  int off_ring, off_op, off_q, off_meta, off_bar, total;
+  int off_ring, off_op, off_q, off_meta, off_scale, off_bar, total;
   int slot_cols, tmem_cols, rows_per_chunk;
 };
 
@@ -75,9 +77,10 @@ __host__ inline Layout make_layout(int fp8, int max_rows) {
     L.stages = (kSmemLimit - fixed) / kOpBytes;
     if (L.stages > 8) L.stages = 8;
   } else {
-    L.stage_bytes = kRawFp8Bytes;
+    // a stage: the e4m3 tile, then its 128 scales (moved by the copy engine too)
+    L.stage_bytes = kRawFp8Bytes + kScaleBytes;
     L.op_bufs = 2;
-    L.stages = (kSmemLimit - fixed - 2 * kOpBytes) / kRawFp8Bytes;
+    L.stages = (kSmemLimit - fixed - 2 * kOpBytes - kScaleRing * kScaleBytes) / L.stage_bytes;
     if (L.stages > 8) L.stages = 8;
   }
   int off = 0;
@@ -89,6 +92,8 @@ __host__ inline Layout make_layout(int fp8, int max_rows) {
   off += q_bytes;
   L.off_meta = off;
   off += meta_bytes;
+  L.off_scale = off;
+  off += fp8 ? kScaleRing * kScaleBytes : 0;
   L.off_bar = off;
   off += bar_bytes;
   L.total = off + 1024;
@@ -197,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // barrier indices
   const int B_KFULL = 0, B_KEMPTY = 8, B_OPFULL = 16, B_OPEMPTY = 18, B_QFULL = 20,
             B_QEMPTY = 21, B_ACCFULL = 22, B_ACCEMPTY = 24, B_PFULL = 26, B_PEMPTY = 28,
-            B_DRAIN = 30;
+            B_DRAIN = 30, B_SFULL = 40;  // 40..47: fp8 scale ring slots
   auto bar = [&](int i) { return smem_u32(bars + i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 32);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 33);
@@ -221,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
     mbar_init(bar(B_DRAIN), 1);
+    for (int i = 0; i < kScaleRing; ++i) mbar_init(bar(B_SFULL + i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -308,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pages[h] = pg;
             slots[h] = t0 % P.page_size;
-            bytes += kFp8 ? 64u * 128u : 2u * kHalfBf16Box;
+            bytes += kFp8 ? 64u * 128u + 64u * 4u : 2u * kHalfBf16Box;
           }
           const uint32_t fb = bar(B_KFULL + stage);
           mbar_arrive_expect_tx(fb, bytes);
@@ -317,6 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (pages[h] < 0) continue;
             if (kFp8) {
               tma_load_3d(dst + h * 8192, &P.kmap[sl], fb, 0, slots[h], pages[h]);
+              // the chunk's 64 token scales (256 B, 16-byte aligned: the scale
+              // array is, and a chunk starts at a multiple of 64 tokens)
+              bulk_copy_g2s(dst + kRawFp8Bytes + h * 256,
+                            P.kscale[sl] + static_cast<long long>(pages[h]) * P.page_size +
+                                slots[h],
+                            256u, fb);
             } else {
               tma_load_3d(dst + h * 8192, &P.kmap[sl], fb, 0, slots[h], pages[h]);
               tma_load_3d(dst + 16384 + h * 8192, &P.kmap[sl], fb, 64, slots[h], pages[h]);
@@ -534,11 +546,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint4 o = e4m3x8_to_f16x8(v);
             *reinterpret_cast<uint4*>(opp + kb * 16384 + r * 128 + ((ch ^ (r & 7)) << 4)) = o;
           }
+          // the tile's token scales go on to the epilogue's ring: the stage is
+          // refilled as soon as this warp pair releases it
+          float* ring = reinterpret_cast<float*>(sbase + L.off_scale) + (u % kScaleRing) * kTileT;
+          if (ok) {
+            const float* sc = reinterpret_cast<const float*>(rawp + kRawFp8Bytes);
+            ring[at] = sc[at];
+            ring[at + 64] = sc[at + 64];
+          }
           fence_proxy_async_smem();
           named_bar_sync(1, 64);
           if (ok && at == 0) {
             mbar_arrive(bar(B_KEMPTY + stage));
             mbar_arrive(bar(B_OPFULL + op));
+            mbar_arrive(bar(B_SFULL + u % kScaleRing));
           }
           if (++stage == L.stages) {
             stage = 0;
@@ -576,14 +597,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const PairMeta& m = meta[pair_j & 1];
         const int sl = wk.pair / P.num_reqs;
-        const int b = wk.pair - sl * P.num_reqs;
         const int t = wk.tile * kTileT + et;
         float kscale = 1.0f;
-        if (kFp8 && t < wk.pi.len) {
-          const int pg = page_of(P, sl, b, t / P.page_size);
-          if (pg >= 0 && pg < P.num_pages[sl])
-            kscale = __ldg(P.kscale[sl] + static_cast<long long>(pg) * P.page_size +
-                           (t % P.page_size));
+        if (kFp8) {
+          // the tile's token scales, handed over by the converting warps
+          if (!mbar_wait(bar(B_SFULL + u % kScaleRing), static_cast<uint32_t>(u / kScaleRing) & 1u,
+                         abort_flag))
+            break;
+          kscale = reinterpret_cast<const float*>(sbase + L.off_scale)[(u % kScaleRing) * kTileT + et];
         }
         float* out_base = P.scores + static_cast<long long>(sl) * P.shard_stride;
         const int nr = wk.pi.nr;

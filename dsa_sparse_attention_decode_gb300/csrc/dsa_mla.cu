@@ -288,240 +288,240 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
         mbar_wait(smem_u32(bars + (tile & 1)), static_cast<uint32_t>(tile >> 1) & 1u, &no_abort);
     }
   } else {
-  // ================================================= compute (warps 0..7)
-  // per-thread state: O accumulators for dims [64*warp, 64*warp+64) of all heads
-  float o[MT][8][4];
+    // ================================================= compute (warps 0..7)
+    // per-thread state: O accumulators for dims [64*warp, 64*warp+64) of all heads
+    float o[MT][8][4];
 #pragma unroll
-  for (int a = 0; a < MT; ++a)
+    for (int a = 0; a < MT; ++a)
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < 8; ++j)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) o[a][j][c] = 0.0f;
-  float m_run[MT][2];
+        for (int c = 0; c < 4; ++c) o[a][j][c] = 0.0f;
+    float m_run[MT][2];
 #pragma unroll
-  for (int a = 0; a < MT; ++a) m_run[a][0] = m_run[a][1] = -__int_as_float(0x7f800000);
-  float l_part[2] = {0.0f, 0.0f};  // row sums of this thread's S rows
+    for (int a = 0; a < MT; ++a) m_run[a][0] = m_run[a][1] = -__int_as_float(0x7f800000);
+    float l_part[2] = {0.0f, 0.0f};  // row sums of this thread's S rows
 
-  const int mt_s = warp % MT;          // S role: head tile
-  const int tg = warp / MT;            // S role: token group
-  const int n_s0 = tg * (8 * NTW);     // first token of the group in the tile
-  const float qsc0 = qexp[mt_s * 16 + g];
-  const float qsc1 = qexp[mt_s * 16 + g + 8];
+    const int mt_s = warp % MT;          // S role: head tile
+    const int tg = warp / MT;            // S role: token group
+    const int n_s0 = tg * (8 * NTW);     // first token of the group in the tile
+    const float qsc0 = qexp[mt_s * 16 + g];
+    const float qsc1 = qexp[mt_s * 16 + g + 8];
 
-  for (int tile = 0; tile < ntiles; ++tile) {
-    const int fb = tile & 1;  // the gathered tile's buffer (raw rows for fp8)
-    // a timed-out wait (abort flag set) computes on whatever is there; the
-    // error word reports it and every barrier below is still passed
-    mbar_wait(smem_u32(bars + fb), static_cast<uint32_t>(tile >> 1) & 1u, abort_flag);
-    const int buf = kFp8 ? 0 : fb;
-    uint8_t* kv = kv_s + buf * kTile * kRowB;
-    if (kFp8) {
-      const uint8_t* rawp = raw_s + fb * kTile * kKvDim;
-      for (int c = tid; c < kTile * 72; c += kCompute) {
-        const int row = c / 72, cc = c - row * 72;
-        const uint2 v = *reinterpret_cast<const uint2*>(rawp + row * kKvDim + cc * 8);
-        uint4 out;
-        __half2_raw h;
-        h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.x & 0xFFFFu), __NV_E4M3);
-        out.x = h.x | (static_cast<uint32_t>(h.y) << 16);
-        h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.x >> 16), __NV_E4M3);
-        out.y = h.x | (static_cast<uint32_t>(h.y) << 16);
-        h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.y & 0xFFFFu), __NV_E4M3);
-        out.z = h.x | (static_cast<uint32_t>(h.y) << 16);
-        h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.y >> 16), __NV_E4M3);
-        out.w = h.x | (static_cast<uint32_t>(h.y) << 16);
-        *reinterpret_cast<uint4*>(kv + row * kRowB + cc * 16) = out;
+    for (int tile = 0; tile < ntiles; ++tile) {
+      const int fb = tile & 1;  // the gathered tile's buffer (raw rows for fp8)
+      // a timed-out wait (abort flag set) computes on whatever is there; the
+      // error word reports it and every barrier below is still passed
+      mbar_wait(smem_u32(bars + fb), static_cast<uint32_t>(tile >> 1) & 1u, abort_flag);
+      const int buf = kFp8 ? 0 : fb;
+      uint8_t* kv = kv_s + buf * kTile * kRowB;
+      if (kFp8) {
+        const uint8_t* rawp = raw_s + fb * kTile * kKvDim;
+        for (int c = tid; c < kTile * 72; c += kCompute) {
+          const int row = c / 72, cc = c - row * 72;
+          const uint2 v = *reinterpret_cast<const uint2*>(rawp + row * kKvDim + cc * 8);
+          uint4 out;
+          __half2_raw h;
+          h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.x & 0xFFFFu), __NV_E4M3);
+          out.x = h.x | (static_cast<uint32_t>(h.y) << 16);
+          h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.x >> 16), __NV_E4M3);
+          out.y = h.x | (static_cast<uint32_t>(h.y) << 16);
+          h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.y & 0xFFFFu), __NV_E4M3);
+          out.z = h.x | (static_cast<uint32_t>(h.y) << 16);
+          h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.y >> 16), __NV_E4M3);
+          out.w = h.x | (static_cast<uint32_t>(h.y) << 16);
+          *reinterpret_cast<uint4*>(kv + row * kRowB + cc * 16) = out;
+        }
+        named_bar_sync(1, kCompute);
+        if (tid == 0) mbar_arrive(smem_u32(bars + 2 + fb));  // the raw buffer is free
       }
-      named_bar_sync(1, kCompute);
-      if (tid == 0) mbar_arrive(smem_u32(bars + 2 + fb));  // the raw buffer is free
-    }
-    const int t0 = tile * kTile;
-    const uint32_t kv_a = smem_u32(kv);
-    const uint32_t q_a = smem_u32(q_s);
+      const int t0 = tile * kTile;
+      const uint32_t kv_a = smem_u32(kv);
+      const uint32_t q_a = smem_u32(q_s);
 
-    // ---- S = q . kv^T for head tile mt_s, tokens n_s0 .. n_s0 + 8*NTW
-    float sacc[NTW][4];
+      // ---- S = q . kv^T for head tile mt_s, tokens n_s0 .. n_s0 + 8*NTW
+      float sacc[NTW][4];
 #pragma unroll
-    for (int j = 0; j < NTW; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.0f;
-    {
-      const uint32_t a_addr = q_a + (mt_s * 16 + (lane & 15)) * kRowB + (lane >> 4) * 16;
+      for (int j = 0; j < NTW; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.0f;
+      {
+        const uint32_t a_addr = q_a + (mt_s * 16 + (lane & 15)) * kRowB + (lane >> 4) * 16;
 #pragma unroll 4
-      for (int kk = 0; kk < kKvDim / 16; ++kk) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(a_addr + kk * 32, a0, a1, a2, a3);
-        if (NTW == 2) {
-          uint32_t b0, b1, b2, b3;
-          const int trow = n_s0 + (lane & 7) + ((lane >> 4) << 3);
-          ldsm_x4(kv_a + trow * kRowB + kk * 32 + ((lane >> 3) & 1) * 16, b0, b1, b2, b3);
-          mma16816<kFp8>(sacc[0], a0, a1, a2, a3, b0, b1);
-          mma16816<kFp8>(sacc[NTW - 1], a0, a1, a2, a3, b2, b3);
-        } else {
-          uint32_t b0, b1;
-          const int trow = n_s0 + (lane & 7);
-          ldsm_x2(kv_a + trow * kRowB + kk * 32 + ((lane >> 3) & 1) * 16, b0, b1);
-          mma16816<kFp8>(sacc[0], a0, a1, a2, a3, b0, b1);
+        for (int kk = 0; kk < kKvDim / 16; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(a_addr + kk * 32, a0, a1, a2, a3);
+          if (NTW == 2) {
+            uint32_t b0, b1, b2, b3;
+            const int trow = n_s0 + (lane & 7) + ((lane >> 4) << 3);
+            ldsm_x4(kv_a + trow * kRowB + kk * 32 + ((lane >> 3) & 1) * 16, b0, b1, b2, b3);
+            mma16816<kFp8>(sacc[0], a0, a1, a2, a3, b0, b1);
+            mma16816<kFp8>(sacc[NTW - 1], a0, a1, a2, a3, b2, b3);
+          } else {
+            uint32_t b0, b1;
+            const int trow = n_s0 + (lane & 7);
+            ldsm_x2(kv_a + trow * kRowB + kk * 32 + ((lane >> 3) & 1) * 16, b0, b1);
+            mma16816<kFp8>(sacc[0], a0, a1, a2, a3, b0, b1);
+          }
         }
       }
-    }
-    // logits in base 2, masked past the split's end
-    float mx0 = -__int_as_float(0x7f800000), mx1 = mx0;
+      // logits in base 2, masked past the split's end
+      float mx0 = -__int_as_float(0x7f800000), mx1 = mx0;
 #pragma unroll
-    for (int j = 0; j < NTW; ++j) {
+      for (int j = 0; j < NTW; ++j) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int tok = n_s0 + 8 * j + 2 * t4 + c;
-        const bool ok = t0 + tok < ntok;
-        float ks = 1.0f;
-        if (kFp8) ks = ok ? kscale_s[t0 + tok] : 0.0f;
-        const float z0 = ok ? sacc[j][c] * qsc0 * ks : -__int_as_float(0x7f800000);
-        const float z1 = ok ? sacc[j][2 + c] * qsc1 * ks : -__int_as_float(0x7f800000);
-        sacc[j][c] = z0;
-        sacc[j][2 + c] = z1;
-        mx0 = fmaxf(mx0, z0);
-        mx1 = fmaxf(mx1, z1);
+        for (int c = 0; c < 2; ++c) {
+          const int tok = n_s0 + 8 * j + 2 * t4 + c;
+          const bool ok = t0 + tok < ntok;
+          float ks = 1.0f;
+          if (kFp8) ks = ok ? kscale_s[t0 + tok] : 0.0f;
+          const float z0 = ok ? sacc[j][c] * qsc0 * ks : -__int_as_float(0x7f800000);
+          const float z1 = ok ? sacc[j][2 + c] * qsc1 * ks : -__int_as_float(0x7f800000);
+          sacc[j][c] = z0;
+          sacc[j][2 + c] = z1;
+          mx0 = fmaxf(mx0, z0);
+          mx1 = fmaxf(mx1, z1);
+        }
       }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      if (t4 == 0) {
+        red[tg * H + mt_s * 16 + g] = mx0;
+        red[tg * H + mt_s * 16 + g + 8] = mx1;
+      }
+      named_bar_sync(1, kCompute);
+      // new running max for every head row this thread touches
+      float alpha[MT][2];
+#pragma unroll
+      for (int a = 0; a < MT; ++a) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int h = a * 16 + g + hh * 8;
+          float tm = red[h];
+#pragma unroll
+          for (int x = 1; x < TGS; ++x) tm = fmaxf(tm, red[x * H + h]);
+          const float mn = fmaxf(m_run[a][hh], tm);
+          const float msafe = (mn == -__int_as_float(0x7f800000)) ? 0.0f : mn;
+          alpha[a][hh] = exp2f(m_run[a][hh] - msafe);
+          m_run[a][hh] = mn;
+        }
+      }
+      // P for the S rows of this warp
+      {
+        const float mA = (m_run[mt_s][0] == -__int_as_float(0x7f800000)) ? 0.0f : m_run[mt_s][0];
+        const float mB = (m_run[mt_s][1] == -__int_as_float(0x7f800000)) ? 0.0f : m_run[mt_s][1];
+        float ls0 = 0.0f, ls1 = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NTW; ++j) {
+          const int tok = n_s0 + 8 * j + 2 * t4;
+          const float p00 = exp2f(sacc[j][0] - mA), p01 = exp2f(sacc[j][1] - mA);
+          const float p10 = exp2f(sacc[j][2] - mB), p11 = exp2f(sacc[j][3] - mB);
+          ls0 += p00 + p01;
+          ls1 += p10 + p11;
+          float v00 = p00, v01 = p01, v10 = p10, v11 = p11;
+          if (kFp8) {
+            const float k0 = (t0 + tok < ntok) ? kscale_s[t0 + tok] : 0.0f;
+            const float k1 = (t0 + tok + 1 < ntok) ? kscale_s[t0 + tok + 1] : 0.0f;
+            v00 *= k0;
+            v01 *= k1;
+            v10 *= k0;
+            v11 *= k1;
+          }
+          const uint32_t h0 = pack2<kFp8>(v00, v01), h1 = pack2<kFp8>(v10, v11);
+          *reinterpret_cast<uint32_t*>(p_s + (mt_s * 16 + g) * kPRowB + tok * 2) = h0;
+          *reinterpret_cast<uint32_t*>(p_s + (mt_s * 16 + g + 8) * kPRowB + tok * 2) = h1;
+          if (!kFp8) {
+            // bf16 keeps 8 significant bits: carry the rounding remainder of P
+            // in a second bf16 operand so that P . v is exact to ~2^-17
+            *reinterpret_cast<uint32_t*>(p_s + (H + mt_s * 16 + g) * kPRowB + tok * 2) =
+                pack2<false>(v00 - __uint_as_float(h0 << 16), v01 - __uint_as_float(h0 & 0xFFFF0000u));
+            *reinterpret_cast<uint32_t*>(p_s + (H + mt_s * 16 + g + 8) * kPRowB + tok * 2) =
+                pack2<false>(v10 - __uint_as_float(h1 << 16), v11 - __uint_as_float(h1 & 0xFFFF0000u));
+          }
+        }
+        l_part[0] = l_part[0] * alpha[mt_s][0] + ls0;
+        l_part[1] = l_part[1] * alpha[mt_s][1] + ls1;
+      }
+      named_bar_sync(1, kCompute);
+
+      // ---- O += P . v for value dims [64*warp, 64*warp + 64)
+#pragma unroll
+      for (int a = 0; a < MT; ++a)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          o[a][j][0] *= alpha[a][0];
+          o[a][j][1] *= alpha[a][0];
+          o[a][j][2] *= alpha[a][1];
+          o[a][j][3] *= alpha[a][1];
+        }
+      {
+        const uint32_t p_a = smem_u32(p_s);
+        const int d0 = warp * 64;
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          uint32_t af[MT][4], al[MT][4];
+#pragma unroll
+          for (int a = 0; a < MT; ++a) {
+            ldsm_x4(p_a + (a * 16 + (lane & 15)) * kPRowB + kk * 32 + (lane >> 4) * 16, af[a][0],
+                    af[a][1], af[a][2], af[a][3]);
+            if (!kFp8)
+              ldsm_x4(p_a + (H + a * 16 + (lane & 15)) * kPRowB + kk * 32 + (lane >> 4) * 16,
+                      al[a][0], al[a][1], al[a][2], al[a][3]);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            uint32_t b0, b1, b2, b3;
+            const int trow = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int dcol = d0 + (j + (lane >> 4)) * 8;
+            ldsm_x4_t(kv_a + trow * kRowB + dcol * 2, b0, b1, b2, b3);
+#pragma unroll
+            for (int a = 0; a < MT; ++a) {
+              mma16816<kFp8>(o[a][j], af[a][0], af[a][1], af[a][2], af[a][3], b0, b1);
+              mma16816<kFp8>(o[a][j + 1], af[a][0], af[a][1], af[a][2], af[a][3], b2, b3);
+              if (!kFp8) {
+                mma16816<false>(o[a][j], al[a][0], al[a][1], al[a][2], al[a][3], b0, b1);
+                mma16816<false>(o[a][j + 1], al[a][0], al[a][1], al[a][2], al[a][3], b2, b3);
+              }
+            }
+          }
+        }
+      }
+      named_bar_sync(1, kCompute);
+      if (!kFp8 && tid == 0) mbar_arrive(smem_u32(bars + 2 + fb));  // the tile's buffer is free
     }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+
+    // ---- softmax denominators: sum the row partials over t4 and token groups
+    float l0 = l_part[0], l1 = l_part[1];
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    float* red2 = red + TGS * H;
     if (t4 == 0) {
-      red[tg * H + mt_s * 16 + g] = mx0;
-      red[tg * H + mt_s * 16 + g + 8] = mx1;
+      red2[tg * H + mt_s * 16 + g] = l0;
+      red2[tg * H + mt_s * 16 + g + 8] = l1;
     }
     named_bar_sync(1, kCompute);
-    // new running max for every head row this thread touches
-    float alpha[MT][2];
+    const int d0 = warp * 64;
 #pragma unroll
     for (int a = 0; a < MT; ++a) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int h = a * 16 + g + hh * 8;
-        float tm = red[h];
+        float l = 0.0f;
 #pragma unroll
-        for (int x = 1; x < TGS; ++x) tm = fmaxf(tm, red[x * H + h]);
-        const float mn = fmaxf(m_run[a][hh], tm);
-        const float msafe = (mn == -__int_as_float(0x7f800000)) ? 0.0f : mn;
-        alpha[a][hh] = exp2f(m_run[a][hh] - msafe);
-        m_run[a][hh] = mn;
-      }
-    }
-    // P for the S rows of this warp
-    {
-      const float mA = (m_run[mt_s][0] == -__int_as_float(0x7f800000)) ? 0.0f : m_run[mt_s][0];
-      const float mB = (m_run[mt_s][1] == -__int_as_float(0x7f800000)) ? 0.0f : m_run[mt_s][1];
-      float ls0 = 0.0f, ls1 = 0.0f;
+        for (int x = 0; x < TGS; ++x) l += red2[x * H + h];
+        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
 #pragma unroll
-      for (int j = 0; j < NTW; ++j) {
-        const int tok = n_s0 + 8 * j + 2 * t4;
-        const float p00 = exp2f(sacc[j][0] - mA), p01 = exp2f(sacc[j][1] - mA);
-        const float p10 = exp2f(sacc[j][2] - mB), p11 = exp2f(sacc[j][3] - mB);
-        ls0 += p00 + p01;
-        ls1 += p10 + p11;
-        float v00 = p00, v01 = p01, v10 = p10, v11 = p11;
-        if (kFp8) {
-          const float k0 = (t0 + tok < ntok) ? kscale_s[t0 + tok] : 0.0f;
-          const float k1 = (t0 + tok + 1 < ntok) ? kscale_s[t0 + tok + 1] : 0.0f;
-          v00 *= k0;
-          v01 *= k1;
-          v10 *= k0;
-          v11 *= k1;
+        for (int j = 0; j < 8; ++j) {
+          float2 v = make_float2(o[a][j][2 * hh] * inv, o[a][j][2 * hh + 1] * inv);
+          *reinterpret_cast<float2*>(out_o + h * kVDim + d0 + 8 * j + 2 * t4) = v;
         }
-        const uint32_t h0 = pack2<kFp8>(v00, v01), h1 = pack2<kFp8>(v10, v11);
-        *reinterpret_cast<uint32_t*>(p_s + (mt_s * 16 + g) * kPRowB + tok * 2) = h0;
-        *reinterpret_cast<uint32_t*>(p_s + (mt_s * 16 + g + 8) * kPRowB + tok * 2) = h1;
-        if (!kFp8) {
-          // bf16 keeps 8 significant bits: carry the rounding remainder of P
-          // in a second bf16 operand so that P . v is exact to ~2^-17
-          *reinterpret_cast<uint32_t*>(p_s + (H + mt_s * 16 + g) * kPRowB + tok * 2) =
-              pack2<false>(v00 - __uint_as_float(h0 << 16), v01 - __uint_as_float(h0 & 0xFFFF0000u));
-          *reinterpret_cast<uint32_t*>(p_s + (H + mt_s * 16 + g + 8) * kPRowB + tok * 2) =
-              pack2<false>(v10 - __uint_as_float(h1 << 16), v11 - __uint_as_float(h1 & 0xFFFF0000u));
-        }
-      }
-      l_part[0] = l_part[0] * alpha[mt_s][0] + ls0;
-      l_part[1] = l_part[1] * alpha[mt_s][1] + ls1;
-    }
-    named_bar_sync(1, kCompute);
-
-    // ---- O += P . v for value dims [64*warp, 64*warp + 64)
-#pragma unroll
-    for (int a = 0; a < MT; ++a)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        o[a][j][0] *= alpha[a][0];
-        o[a][j][1] *= alpha[a][0];
-        o[a][j][2] *= alpha[a][1];
-        o[a][j][3] *= alpha[a][1];
-      }
-    {
-      const uint32_t p_a = smem_u32(p_s);
-      const int d0 = warp * 64;
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        uint32_t af[MT][4], al[MT][4];
-#pragma unroll
-        for (int a = 0; a < MT; ++a) {
-          ldsm_x4(p_a + (a * 16 + (lane & 15)) * kPRowB + kk * 32 + (lane >> 4) * 16, af[a][0],
-                  af[a][1], af[a][2], af[a][3]);
-          if (!kFp8)
-            ldsm_x4(p_a + (H + a * 16 + (lane & 15)) * kPRowB + kk * 32 + (lane >> 4) * 16,
-                    al[a][0], al[a][1], al[a][2], al[a][3]);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          uint32_t b0, b1, b2, b3;
-          const int trow = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int dcol = d0 + (j + (lane >> 4)) * 8;
-          ldsm_x4_t(kv_a + trow * kRowB + dcol * 2, b0, b1, b2, b3);
-#pragma unroll
-          for (int a = 0; a < MT; ++a) {
-            mma16816<kFp8>(o[a][j], af[a][0], af[a][1], af[a][2], af[a][3], b0, b1);
-            mma16816<kFp8>(o[a][j + 1], af[a][0], af[a][1], af[a][2], af[a][3], b2, b3);
-            if (!kFp8) {
-              mma16816<false>(o[a][j], al[a][0], al[a][1], al[a][2], al[a][3], b0, b1);
-              mma16816<false>(o[a][j + 1], al[a][0], al[a][1], al[a][2], al[a][3], b2, b3);
-            }
-          }
+        if (warp == 0 && t4 == 0) {
+          out_l[h] = l > 0.0f ? (m_run[a][hh] + log2f(l)) * kLn2 : -__int_as_float(0x7f800000);
         }
       }
     }
-    named_bar_sync(1, kCompute);
-    if (!kFp8 && tid == 0) mbar_arrive(smem_u32(bars + 2 + fb));  // the tile's buffer is free
-  }
-
-  // ---- softmax denominators: sum the row partials over t4 and token groups
-  float l0 = l_part[0], l1 = l_part[1];
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  float* red2 = red + TGS * H;
-  if (t4 == 0) {
-    red2[tg * H + mt_s * 16 + g] = l0;
-    red2[tg * H + mt_s * 16 + g + 8] = l1;
-  }
-  named_bar_sync(1, kCompute);
-  const int d0 = warp * 64;
-#pragma unroll
-  for (int a = 0; a < MT; ++a) {
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const int h = a * 16 + g + hh * 8;
-      float l = 0.0f;
-#pragma unroll
-      for (int x = 0; x < TGS; ++x) l += red2[x * H + h];
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float2 v = make_float2(o[a][j][2 * hh] * inv, o[a][j][2 * hh + 1] * inv);
-        *reinterpret_cast<float2*>(out_o + h * kVDim + d0 + 8 * j + 2 * t4) = v;
-      }
-      if (warp == 0 && t4 == 0) {
-        out_l[h] = l > 0.0f ? (m_run[a][hh] + log2f(l)) * kLn2 : -__int_as_float(0x7f800000);
-      }
-    }
-  }
   }
 
   __syncthreads();
