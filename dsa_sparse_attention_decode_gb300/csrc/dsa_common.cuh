@@ -207,6 +207,17 @@ DSA_DEV void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint3
       : "memory");
 }
 
+// D (+)= A . B^T with e4m3 operands (both the same type) and an fp32 accumulator
+DSA_DEV void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // arrive once on the mbarrier when all prior tcgen05 async ops of this thread end
 DSA_DEV void tc_commit(uint32_t bar) {
   asm volatile(
@@ -267,6 +278,12 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_bf16, int b
   return (1u << 4) | (static_cast<uint32_t>(a_bf16) << 7) |
          (static_cast<uint32_t>(b_bf16) << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format code 0 for
+// both), f32 accumulator, K-major operands.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // ----------------------------------------------------------------- misc

@@ -11,12 +11,18 @@
 //   warp 1      tcgen05 issuer: D[128 tokens x 64*rows] = K_tile . Q^T with
 //               the accumulator in TMEM (two slots, so the epilogue of one
 //               tile overlaps the MMA of the next).
-//   warps 2-3   Q staging (bf16 as is; for fp8 keys the query is turned into
-//               f16 with a per-head power-of-two scale) and, for fp8 keys, the
-//               e4m3 -> f16 conversion of each tile into the operand buffer.
+//   warps 2-3   Q staging.  bf16 keys: the query as is (kind::f16).  fp8
+//               keys: the MMA runs kind::f8f6f4 on the e4m3 tile as it lands,
+//               and each head's query, scaled by 2^e so that its largest |q|
+//               sits in [224, 448], is split into two e4m3 terms hi + lo (lo
+//               holds the rounding remainder of hi; together they keep every
+//               bf16 digit down to 2^-9 at that scale) that accumulate into
+//               the same TMEM columns; 2^-e goes into the head weight.
 //   warps 4-7   epilogue: one thread per token row of the tile reads its
 //               TMEM lane, applies relu, the head weights (and the fp8
-//               per-token scale) and stores the fp32 score.
+//               per-token scale, read from the key stage, which is released
+//               only once the MMA and the four epilogue warps are done with
+//               it) and stores the fp32 score.
 // Work units are (shard, request, tile); the flattened unit list is split
 // evenly over the CTAs.  All rows of a request share one key stream.
 #include <cuda_fp16.h>
@@ -30,10 +36,11 @@ namespace {
 
 constexpr int kTileT = 128;
 constexpr int kThreads = 256;
-constexpr int kOpBytes = kTileT * kIdxDim * 2;     // 32 KB f16/bf16 operand tile
-constexpr int kRawFp8Bytes = kTileT * kIdxDim;     // 16 KB e4m3 tile
-constexpr int kScaleBytes = kTileT * 4;            // the tile's fp32 token scales
-constexpr int kScaleRing = 8;                      // fp8: tiles of scales kept for the epilogue
+constexpr int kOpBytes = kTileT * kIdxDim * 2;     // 32 KB bf16 key tile
+constexpr int kRawFp8Bytes = kTileT * kIdxDim;     // 16 KB e4m3 key tile
+// an fp8 stage: the e4m3 tile, its 128 fp32 token scales, padding to the
+// 1024-byte alignment of the 128B-swizzled operand
+constexpr int kFp8StageBytes = kRawFp8Bytes + 1024;
 constexpr int kHalfBf16Box = 64 * 64 * 2;          // one TMA box: 64 tokens x 64 dims
 constexpr int kSmemLimit = 227 * 1024;
 
@@ -45,11 +52,10 @@ struct PairMeta {           // per (shard, request) pair, written by the aux war
 
 struct Layout {
   int stages;      // TMA ring depth
-  int op_bufs;     // fp8 operand buffers
   int stage_bytes;
   int q_rows;      // max_rows * 64
   int q_kb_stride; // bytes between the two 64-dim halves of Q
-  int off_ring, off_op, off_q, off_meta, off_scale, off_bar, total;
+  int off_ring, off_q, off_meta, off_bar, total;
   int slot_cols, tmem_cols, rows_per_chunk;
 };
 
@@ -71,29 +77,16 @@ __host__ inline Layout make_layout(int fp8, int max_rows) {
   const int meta_bytes = 2 * static_cast<int>(sizeof(PairMeta));
   const int bar_bytes = 512;
   const int fixed = 1024 /*align*/ + q_bytes + meta_bytes + bar_bytes;
-  if (!fp8) {
-    L.stage_bytes = kOpBytes;
-    L.op_bufs = 0;
-    L.stages = (kSmemLimit - fixed) / kOpBytes;
-    if (L.stages > 8) L.stages = 8;
-  } else {
-    // a stage: the e4m3 tile, then its 128 scales (moved by the copy engine too)
-    L.stage_bytes = kRawFp8Bytes + kScaleBytes;
-    L.op_bufs = 2;
-    L.stages = (kSmemLimit - fixed - 2 * kOpBytes - kScaleRing * kScaleBytes) / L.stage_bytes;
-    if (L.stages > 8) L.stages = 8;
-  }
+  L.stage_bytes = fp8 ? kFp8StageBytes : kOpBytes;
+  L.stages = (kSmemLimit - fixed) / L.stage_bytes;
+  if (L.stages > 8) L.stages = 8;
   int off = 0;
   L.off_ring = off;
   off += L.stages * L.stage_bytes;
-  L.off_op = off;
-  off += L.op_bufs * kOpBytes;
   L.off_q = off;
   off += q_bytes;
   L.off_meta = off;
   off += meta_bytes;
-  L.off_scale = off;
-  off += fp8 ? kScaleRing * kScaleBytes : 0;
   L.off_bar = off;
   off += bar_bytes;
   L.total = off + 1024;
@@ -171,19 +164,17 @@ __device__ __forceinline__ int page_of(const IndexerLaunch& P, int sl, int b, in
             : b * P.max_blocks[sl] + lp;
 }
 
-// e4m3 x 8 -> f16 x 8 (exact: every e4m3 value is an f16 value)
-__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 v) {
-  uint4 o;
-  __half2_raw h;
-  h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.x & 0xFFFFu), __NV_E4M3);
-  o.x = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-  h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.x >> 16), __NV_E4M3);
-  o.y = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-  h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.y & 0xFFFFu), __NV_E4M3);
-  o.z = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-  h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v.y >> 16), __NV_E4M3);
-  o.w = static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-  return o;
+// Two e4m3 terms of a float pair (a, b): hi = e4m3(x), lo = e4m3(x - hi),
+// each packed as two bytes with a in the low byte.
+__device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_fp8x2_storage_t h =
+      __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3);
+  const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  const __nv_fp8x2_storage_t l =
+      __nv_cvt_float2_to_fp8x2(make_float2(a - back.x, b - back.y), __NV_SATFINITE, __NV_E4M3);
+  hi = static_cast<uint32_t>(h);
+  lo = static_cast<uint32_t>(l);
 }
 
 template <bool kFp8>
@@ -200,9 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + L.off_bar);
   // barrier indices
-  const int B_KFULL = 0, B_KEMPTY = 8, B_OPFULL = 16, B_OPEMPTY = 18, B_QFULL = 20,
-            B_QEMPTY = 21, B_ACCFULL = 22, B_ACCEMPTY = 24, B_PFULL = 26, B_PEMPTY = 28,
-            B_DRAIN = 30, B_SFULL = 40;  // 40..47: fp8 scale ring slots
+  const int B_KFULL = 0, B_KEMPTY = 8, B_QFULL = 20, B_QEMPTY = 21, B_ACCFULL = 22,
+            B_ACCEMPTY = 24, B_PFULL = 26, B_PEMPTY = 28, B_DRAIN = 30;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 32);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 33);
@@ -213,11 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < L.stages; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
-      mbar_init(bar(B_KEMPTY + s), 1);
+      // fp8: the MMA commit and one arrival per epilogue warp (token scales)
+      mbar_init(bar(B_KEMPTY + s), kFp8 ? 5 : 1);
     }
     for (int o = 0; o < 2; ++o) {
-      mbar_init(bar(B_OPFULL + o), 1);
-      mbar_init(bar(B_OPEMPTY + o), 1);
       mbar_init(bar(B_ACCFULL + o), 1);
       mbar_init(bar(B_ACCEMPTY + o), 128);
       mbar_init(bar(B_PFULL + o), 1);
@@ -226,7 +215,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
     mbar_init(bar(B_DRAIN), 1);
-    for (int i = 0; i < kScaleRing; ++i) mbar_init(bar(B_SFULL + i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -286,7 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int start_pair = s_start[0];
     const int start_tile = s_start[1];
     const uint32_t ring = base + L.off_ring;
-    const uint32_t opbase = base + L.off_op;
     const uint32_t qbase = base + L.off_q;
 
     if (warp == 0) {
@@ -340,10 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           wk.next(P);
         }
-        // bf16: the stage releases are tcgen05 commits whose arrivals land
+        // the stage releases include tcgen05 commits whose arrivals land
         // asynchronously; the last one of every stage must have landed before
         // the CTA exits, or it could reach the shared memory of a later CTA
-        if (!kFp8 && !*abort_flag) {
+        if (!*abort_flag) {
           for (int s = 0; s < L.stages && s < issued; ++s) {
             const int last = s + ((issued - 1 - s) / L.stages) * L.stages;
             mbar_wait(bar(B_KEMPTY + s), static_cast<uint32_t>(last / L.stages) & 1u, abort_flag);
@@ -367,8 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         wk.start(P, start_pair, start_tile);
         int stage = 0;
         uint32_t phase = 0;
-        int op = 0;
-        uint32_t op_phase = 0;
         uint32_t acc_iter = 0;
         int pair_j = -1, last_pair = -1;
         for (int u = 0; u < nunits; ++u) {
@@ -379,14 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(bar(B_QFULL), static_cast<uint32_t>(pair_j) & 1u, abort_flag)) break;
             tc_fence_after();
           }
-          uint32_t a_base;
-          if (kFp8) {
-            if (!mbar_wait(bar(B_OPFULL + op), op_phase, abort_flag)) break;
-            a_base = opbase + op * kOpBytes;
-          } else {
-            if (!mbar_wait(bar(B_KFULL + stage), phase, abort_flag)) break;
-            a_base = ring + stage * L.stage_bytes;
-          }
+          if (!mbar_wait(bar(B_KFULL + stage), phase, abort_flag)) break;
+          const uint32_t a_base = ring + stage * L.stage_bytes;
           tc_fence_after();
           const int nr = wk.pi.nr;
           const int rpc = L.rows_per_chunk;
@@ -401,33 +380,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t d = tmem_base + static_cast<uint32_t>(slot * L.slot_cols);
-            const uint32_t idesc = idesc_f16(128, rows_c * kIdxHeads, kFp8 ? 0 : 1, kFp8 ? 0 : 1);
+            const uint32_t idesc = kFp8 ? idesc_e4m3(128, rows_c * kIdxHeads)
+                                        : idesc_f16(128, rows_c * kIdxHeads, 1, 1);
             const uint32_t b_base = qbase + static_cast<uint32_t>(c0 * kIdxHeads * 128);
+            // bf16: kb walks the two 64-dim halves of keys and query.
+            // fp8: the 128-dim e4m3 tile is one 128-byte row per token, met
+            // once by the hi terms of the query (kb 0) and once by the lo
+            // terms (kb 1), both into the same accumulator.
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const uint64_t ad = smem_desc_sw128(a_base + kb * 16384 + k * 32);
+                const uint64_t ad = smem_desc_sw128(a_base + (kFp8 ? 0 : kb * 16384) + k * 32);
                 const uint64_t bd = smem_desc_sw128(b_base + kb * L.q_kb_stride + k * 32);
-                tc_mma_f16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                if (kFp8)
+                  tc_mma_f8(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                else
+                  tc_mma_f16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
               }
             }
             tc_commit(bar(B_ACCFULL + slot));
             ++acc_iter;
           }
           if (!ok) break;
-          if (kFp8) {
-            tc_commit(bar(B_OPEMPTY + op));
-            if (++op == 2) {
-              op = 0;
-              op_phase ^= 1u;
-            }
-          } else {
-            tc_commit(bar(B_KEMPTY + stage));
-            if (++stage == L.stages) {
-              stage = 0;
-              phase ^= 1u;
-            }
+          tc_commit(bar(B_KEMPTY + stage));
+          if (++stage == L.stages) {
+            stage = 0;
+            phase ^= 1u;
           }
           wk.next(P);
         }
@@ -437,14 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar(B_DRAIN), 0u, &no_abort);
       }
     } else if (warp == 2 || warp == 3) {
-      // ------------------------------------------------ Q staging / fp8 convert
+      // ------------------------------------------------ Q staging
       const int at = tid - 64;  // 0..63
       Walker wk;
       wk.start(P, start_pair, start_tile);
-      int stage = 0;
-      uint32_t phase = 0;
-      int op = 0;
-      uint32_t op_phase = 0;
       int pair_j = -1, last_pair = -1;
       // A failed (timed-out) wait stops the work of this thread but it keeps
       // passing the same named barriers as its partner warp.
@@ -474,10 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 16; ++c) v[c] = __ldg(src + c);
             float wv = __ldg(P.w_idx + static_cast<long long>(row0 + g) * kIdxHeads + h);
+            const uint32_t qrow = static_cast<uint32_t>(L.off_q + n * 128);
             if (kFp8) {
               // scale the head's query by 2^e so that its largest |q| lands in
-              // [2^14, 2^15): every bf16 value then converts to f16 exactly
-              // (up to values 2^29 times smaller than that maximum)
+              // [224, 448] (the top of the e4m3 range), then split every value
+              // x into hi = e4m3(x) and lo = e4m3(x - hi)
               uint32_t mx = 0;
 #pragma unroll
               for (int c = 0; c < 16; ++c) {
@@ -488,32 +464,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                   mx = max(mx, (wds[j] >> 16) & 0x7FFFu);
                 }
               }
-              const int ebits = static_cast<int>(mx >> 7);  // biased exponent of max
-              const int e = (ebits == 0) ? 0 : max(-100, min(100, 141 - ebits));
+              // mx is the bf16 pattern of the largest |q|: biased exponent in
+              // bits 7..14, mantissa in bits 0..6 (0x60 = 1.75, i.e. 448 / 256)
+              const int ebits = static_cast<int>(mx >> 7);
+              const int e = (ebits == 0)
+                                ? 0
+                                : max(-100, min(100, ((mx & 0x7Fu) <= 0x60u ? 135 : 134) - ebits));
               const float sc = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
               wv = wv * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
 #pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const uint32_t* wds = reinterpret_cast<const uint32_t*>(&v[c]);
-                uint32_t o[4];
+              for (int ch = 0; ch < 8; ++ch) {
+                // 16 dims: the 8 bf16 pairs of v[2ch] and v[2ch + 1]
+                const uint32_t* wds = reinterpret_cast<const uint32_t*>(&v[2 * ch]);
+                uint32_t ho[4], lo[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const float lo = __uint_as_float(wds[j] << 16) * sc;
-                  const float hi = __uint_as_float(wds[j] & 0xFFFF0000u) * sc;
-                  __half2 hh = __floats2half2_rn(lo, hi);
-                  o[j] = *reinterpret_cast<uint32_t*>(&hh);
+                for (int q = 0; q < 4; ++q) {
+                  uint32_t h0, l0, h1, l1;
+                  const uint32_t wa = wds[2 * q], wb = wds[2 * q + 1];
+                  split_e4m3x2(__uint_as_float(wa << 16) * sc, __uint_as_float(wa & 0xFFFF0000u) * sc,
+                               h0, l0);
+                  split_e4m3x2(__uint_as_float(wb << 16) * sc, __uint_as_float(wb & 0xFFFF0000u) * sc,
+                               h1, l1);
+                  ho[q] = h0 | (h1 << 16);
+                  lo[q] = l0 | (l1 << 16);
                 }
-                v[c] = make_uint4(o[0], o[1], o[2], o[3]);
+                const uint32_t off = qrow + static_cast<uint32_t>((ch ^ (n & 7)) << 4);
+                *reinterpret_cast<uint4*>(sbase + off) = make_uint4(ho[0], ho[1], ho[2], ho[3]);
+                *reinterpret_cast<uint4*>(sbase + off + L.q_kb_stride) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
               }
-            }
-            // store into the K-major 128B-swizzled operand layout
+            } else {
+              // the K-major 128B-swizzled operand layout, 64 dims per half
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int kb = c >> 3;
-              const int ch = c & 7;
-              const uint32_t off = static_cast<uint32_t>(kb * L.q_kb_stride + n * 128 +
-                                                         ((ch ^ (n & 7)) << 4));
-              *reinterpret_cast<uint4*>(sbase + L.off_q + off) = v[c];
+              for (int c = 0; c < 16; ++c) {
+                const int kb = c >> 3;
+                const int ch = c & 7;
+                const uint32_t off = qrow + static_cast<uint32_t>(kb * L.q_kb_stride + ((ch ^ (n & 7)) << 4));
+                *reinterpret_cast<uint4*>(sbase + off) = v[c];
+              }
             }
             m.w[g][h] = wv;
           }
@@ -529,54 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(bar(B_PFULL + mslot));
           }
         }
-        if (kFp8) {
-          // convert the raw e4m3 tile into the f16 operand buffer
-          if (ok) ok = mbar_wait(bar(B_KFULL + stage), phase, abort_flag);
-          if (ok) ok = mbar_wait(bar(B_OPEMPTY + op), op_phase ^ 1u, abort_flag);
-          const uint8_t* rawp = sbase + L.off_ring + stage * L.stage_bytes;
-          uint8_t* opp = sbase + L.off_op + op * kOpBytes;
-          const int wi = at >> 5;  // 0..1
-          const int l16 = lane & 15;
-          const int kb = l16 >> 3;
-          const int ch = l16 & 7;
-#pragma unroll 4
-          for (int it = 0; ok && it < 32; ++it) {
-            const int r = (it * 2 + wi) * 2 + (lane >> 4);
-            const uint2 v = *reinterpret_cast<const uint2*>(rawp + r * 128 + l16 * 8);
-            const uint4 o = e4m3x8_to_f16x8(v);
-            *reinterpret_cast<uint4*>(opp + kb * 16384 + r * 128 + ((ch ^ (r & 7)) << 4)) = o;
-          }
-          // the tile's token scales go on to the epilogue's ring: the stage is
-          // refilled as soon as this warp pair releases it
-          float* ring = reinterpret_cast<float*>(sbase + L.off_scale) + (u % kScaleRing) * kTileT;
-          if (ok) {
-            const float* sc = reinterpret_cast<const float*>(rawp + kRawFp8Bytes);
-            ring[at] = sc[at];
-            ring[at + 64] = sc[at + 64];
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(1, 64);
-          if (ok && at == 0) {
-            mbar_arrive(bar(B_KEMPTY + stage));
-            mbar_arrive(bar(B_OPFULL + op));
-            mbar_arrive(bar(B_SFULL + u % kScaleRing));
-          }
-          if (++stage == L.stages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          if (++op == 2) {
-            op = 0;
-            op_phase ^= 1u;
-          }
-        }
         wk.next(P);
-      }
-      // the operand buffers' last releases are tcgen05 commits whose arrivals
-      // land asynchronously: wait for them before the CTA can exit
-      if (kFp8 && ok && at == 0) {
-        for (int u = max(0, nunits - 2); u < nunits; ++u)
-          mbar_wait(bar(B_OPEMPTY + (u & 1)), static_cast<uint32_t>(u >> 1) & 1u, abort_flag);
       }
     } else {
       // ------------------------------------------------ epilogue (warps 4..7)
@@ -585,26 +526,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       Walker wk;
       wk.start(P, start_pair, start_tile);
       uint32_t acc_iter = 0;
+      int stage = 0;
+      uint32_t phase = 0;
       int pair_j = -1, last_pair = -1;
       for (int u = 0; u < nunits; ++u) {
         if (wk.pair != last_pair) {
           if (pair_j >= 0) mbar_arrive(bar(B_PEMPTY + (pair_j & 1)));
           ++pair_j;
           last_pair = wk.pair;
-          if (!mbar_wait(bar(B_PFULL + (pair_j & 1)), static_cast<uint32_t>(pair_j >> 1) & 1u,
-                         abort_flag))
-            break;
+          const bool got = mbar_wait(bar(B_PFULL + (pair_j & 1)),
+                                     static_cast<uint32_t>(pair_j >> 1) & 1u, abort_flag);
+          if (!__all_sync(0xffffffffu, got)) break;
         }
         const PairMeta& m = meta[pair_j & 1];
         const int sl = wk.pair / P.num_reqs;
         const int t = wk.tile * kTileT + et;
         float kscale = 1.0f;
         if (kFp8) {
-          // the tile's token scales, handed over by the converting warps
-          if (!mbar_wait(bar(B_SFULL + u % kScaleRing), static_cast<uint32_t>(u / kScaleRing) & 1u,
-                         abort_flag))
-            break;
-          kscale = reinterpret_cast<const float*>(sbase + L.off_scale)[(u % kScaleRing) * kTileT + et];
+          // the tile's token scales sit behind its keys in the stage, which
+          // stays filled until this warp's release below
+          const bool got = mbar_wait(bar(B_KFULL + stage), phase, abort_flag);
+          if (!__all_sync(0xffffffffu, got)) break;
+          kscale = reinterpret_cast<const float*>(sbase + L.off_ring + stage * L.stage_bytes +
+                                                  kRawFp8Bytes)[et];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_KEMPTY + stage));
+          if (++stage == L.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
         float* out_base = P.scores + static_cast<long long>(sl) * P.shard_stride;
         const int nr = wk.pi.nr;
