@@ -421,7 +421,9 @@ def run_product(args):
     torch.cuda.synchronize()
     if api.dsa_read_error(err) != 0:
         raise SystemExit("device error word set")
-    kern_us = {n: 1e3 * float(np.mean(v)) for n, v in kern.items()}
+    # median: one launch delayed by the host (the events bracket it) must not
+    # skew the per-kernel figures
+    kern_us = {n: 1e3 * float(np.median(v)) for n, v in kern.items()}
 
     # ---- end to end through the C ABI with host buffers
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())  # noqa: E731

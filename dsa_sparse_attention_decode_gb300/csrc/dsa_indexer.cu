@@ -203,8 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < L.stages; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
-      // fp8: the MMA commit and one arrival per epilogue warp (token scales)
-      mbar_init(bar(B_KEMPTY + s), kFp8 ? 5 : 1);
+      // released by the four epilogue warps once the tile's last
+      // accumulator has landed (its MMAs, which read the stage, are done)
+      mbar_init(bar(B_KEMPTY + s), 4);
     }
     for (int o = 0; o < 2; ++o) {
       mbar_init(bar(B_ACCFULL + o), 1);
@@ -327,9 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           wk.next(P);
         }
-        // the stage releases include tcgen05 commits whose arrivals land
-        // asynchronously; the last one of every stage must have landed before
-        // the CTA exits, or it could reach the shared memory of a later CTA
+        // every stage's last release before the CTA exits (the epilogue is
+        // behind this thread), so that no barrier is left mid-phase
         if (!*abort_flag) {
           for (int s = 0; s < L.stages && s < issued; ++s) {
             const int last = s + ((issued - 1 - s) / L.stages) * L.stages;
@@ -403,7 +403,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++acc_iter;
           }
           if (!ok) break;
-          tc_commit(bar(B_KEMPTY + stage));
           if (++stage == L.stages) {
             stage = 0;
             phase ^= 1u;
@@ -549,12 +548,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!__all_sync(0xffffffffu, got)) break;
           kscale = reinterpret_cast<const float*>(sbase + L.off_ring + stage * L.stage_bytes +
                                                   kRawFp8Bytes)[et];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_KEMPTY + stage));
-          if (++stage == L.stages) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
         float* out_base = P.scores + static_cast<long long>(sl) * P.shard_stride;
         const int nr = wk.pi.nr;
@@ -577,12 +570,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_32x32b_x32(taddr, v0);
             tmem_ld_32x32b_x32(taddr + 32, v1);
             tmem_wait_ld();
-            float s = 0.0f;
+            // eight independent partial sums: one warp per scheduler has no
+            // other work to hide a 64-long dependent chain behind
+            float ps[8];
 #pragma unroll
-            for (int h = 0; h < 32; ++h) s = fmaf(m.w[g][h], fmaxf(__uint_as_float(v0[h]), 0.0f), s);
+            for (int j = 0; j < 8; ++j) ps[j] = 0.0f;
 #pragma unroll
             for (int h = 0; h < 32; ++h)
-              s = fmaf(m.w[g][32 + h], fmaxf(__uint_as_float(v1[h]), 0.0f), s);
+              ps[h & 7] = fmaf(m.w[g][h], fmaxf(__uint_as_float(v0[h]), 0.0f), ps[h & 7]);
+#pragma unroll
+            for (int h = 0; h < 32; ++h)
+              ps[h & 7] = fmaf(m.w[g][32 + h], fmaxf(__uint_as_float(v1[h]), 0.0f), ps[h & 7]);
+            const float s = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             if (t < m.valid[g]) {
               out_base[static_cast<long long>(m.row[g]) * P.ld + t] = s * kscale;
             }
@@ -592,6 +591,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++acc_iter;
         }
         if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_KEMPTY + stage));
+        if (++stage == L.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
         wk.next(P);
       }
     }

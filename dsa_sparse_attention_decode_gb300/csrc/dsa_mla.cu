@@ -33,6 +33,8 @@ constexpr int kCompute = 256;                 // warps 0..7: tensor-core math
 constexpr int kGather = 64;                   // warps 8..9: the row gather
 constexpr int kThreads = kCompute + kGather;
 constexpr int kTile = 64;                 // tokens per tile
+constexpr int kMaxK = 4096;               // largest selection the entry points accept
+constexpr int kMaxPerThread = (kMaxK + kThreads - 1) / kThreads;
 constexpr int kRowB = kKvDim * 2 + 16;    // padded smem row of 576 16-bit values
 constexpr int kPRowB = kTile * 2 + 16;    // padded smem row of P
 constexpr float kLog2e = 1.4426950408889634f;
@@ -164,23 +166,32 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
     return;
   }
 
-  // request of this row
+  // bf16 query -> smem, in flight while the positions are looked up
+  const uint16_t* qsrc = P.q + static_cast<long long>(r) * H * kKvDim;
+  if (!kFp8) {
+    for (int c = tid; c < H * 72; c += kThreads) {
+      const int h = c / 72, cc = c - h * 72;
+      cp_async16(smem_u32(q_s + h * kRowB + cc * 16), qsrc + h * kKvDim + cc * 8);
+    }
+    cp_async_commit();
+  }
+
+  // the split's selected positions: all loads issued before any is used
+  const int32_t* ilist = P.idx + static_cast<long long>(qrow) * P.k + begin;
+  int tv[kMaxPerThread];
+#pragma unroll
+  for (int j = 0; j < kMaxPerThread; ++j) {
+    const int i = tid + j * kThreads;
+    tv[j] = i < ntok ? __ldg(ilist + i) : 0;
+  }
+  // request of this row: the one i with row_start[i] <= r < row_start[i + 1]
+  // (row_start is non-decreasing, so at most one non-empty request matches)
+  if (tid == 0) misc[0] = -1;
+  __syncthreads();
+  for (int i = tid; i < P.num_reqs; i += kThreads) {
+    if (__ldg(P.row_start + i) <= r && r < __ldg(P.row_start + i + 1)) misc[0] = i;
+  }
   if (tid == 0) {
-    int lo = 0, hi = P.num_reqs - 1, b = -1;
-    while (lo <= hi) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldg(P.row_start + mid) <= r) {
-        b = mid;
-        lo = mid + 1;
-      } else {
-        hi = mid - 1;
-      }
-    }
-    if (b < 0 || r >= __ldg(P.row_start + b + 1)) {
-      raise_err(P.d_err, DSA_DEVERR_ROWS);
-      b = -1;
-    }
-    misc[0] = b;
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(bars + i), kGather);   // tile landed: every gather thread's copies
       mbar_init(smem_u32(bars + 2 + i), 1);     // buffer free: one compute thread
@@ -189,14 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
     fence_mbar_init();
   }
 
-  // query -> smem (bf16 copy; fp8 path: f16 with a per-head power of two)
-  const uint16_t* qsrc = P.q + static_cast<long long>(r) * H * kKvDim;
+  // bf16: wait for the query copy; fp8: the query as f16 with a per-head
+  // power of two
   if (!kFp8) {
-    for (int c = tid; c < H * 72; c += kThreads) {
-      const int h = c / 72, cc = c - h * 72;
-      cp_async16(smem_u32(q_s + h * kRowB + cc * 16), qsrc + h * kKvDim + cc * 8);
-    }
-    cp_async_commit();
     cp_async_wait<0>();
     if (tid < H) qexp[tid] = P.sm_scale * kLog2e;
   } else {
@@ -221,29 +227,47 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
     }
   }
   __syncthreads();
-
-  // resolve the split's positions to element offsets
   const int b = misc[0];
+  if (tid == 0 && b < 0) raise_err(P.d_err, DSA_DEVERR_ROWS);
+
+  // resolve the positions to element offsets: block-table loads in one batch,
+  // then (fp8) the token scales in one batch
   const int32_t* bt = P.block_table[w];
   const int psz = P.page_size;
-  const int32_t* ilist = P.idx + static_cast<long long>(qrow) * P.k + begin;
-  for (int i = tid; i < ntok; i += kThreads) {
-    const int t = __ldg(ilist + i);
-    long long off = -1;
-    if (b >= 0 && t >= 0 && static_cast<long long>(t) < static_cast<long long>(P.max_blocks[w]) * psz) {
-      const int lp = t / psz;
-      const int pg = bt ? __ldg(bt + static_cast<long long>(b) * P.max_blocks[w] + lp)
-                        : b * P.max_blocks[w] + lp;
-      if (pg >= 0 && pg < P.num_pages[w]) {
-        off = static_cast<long long>(pg) * psz + (t - lp * psz);
+  const long long span = static_cast<long long>(P.max_blocks[w]) * psz;
+  long long offv[kMaxPerThread];
+#pragma unroll
+  for (int j = 0; j < kMaxPerThread; ++j) {
+    const int i = tid + j * kThreads;
+    offv[j] = -1;
+    if (i < ntok) {
+      const int t = tv[j];
+      if (b >= 0 && t >= 0 && static_cast<long long>(t) < span) {
+        const int lp = t / psz;
+        const int pg = bt ? __ldg(bt + static_cast<long long>(b) * P.max_blocks[w] + lp)
+                          : b * P.max_blocks[w] + lp;
+        offv[j] = static_cast<long long>(pg) * psz + (t - lp * psz);
+        tv[j] = pg;
       } else {
-        raise_err(P.d_err, DSA_DEVERR_PAGE);
+        raise_err(P.d_err, DSA_DEVERR_INDEX);
       }
-    } else {
-      raise_err(P.d_err, DSA_DEVERR_INDEX);
     }
-    rowoff[i] = off;
-    if (kFp8) kscale_s[i] = off >= 0 ? __ldg(P.kscale[w] + off) : 0.0f;
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxPerThread; ++j) {
+    const int i = tid + j * kThreads;
+    if (i < ntok && offv[j] >= 0 && (tv[j] < 0 || tv[j] >= P.num_pages[w])) {
+      raise_err(P.d_err, DSA_DEVERR_PAGE);
+      offv[j] = -1;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxPerThread; ++j) {
+    const int i = tid + j * kThreads;
+    if (i < ntok) {
+      rowoff[i] = offv[j];
+      if (kFp8) kscale_s[i] = offv[j] >= 0 ? __ldg(P.kscale[w] + offv[j]) : 0.0f;
+    }
   }
   __syncthreads();
 
@@ -340,28 +364,44 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
       const uint32_t q_a = smem_u32(q_s);
 
       // ---- S = q . kv^T for head tile mt_s, tokens n_s0 .. n_s0 + 8*NTW
+      // Software-pipelined: the fragments of step kk + 1 are requested before
+      // the MMAs of step kk issue (the asm statements keep program order), and
+      // even and odd steps accumulate into separate registers so that no MMA
+      // waits for the one just before it.
       float sacc[NTW][4];
-#pragma unroll
-      for (int j = 0; j < NTW; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.0f;
       {
+        float sacc2[2][NTW][4];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+          for (int j = 0; j < NTW; ++j)
+            sacc2[h2][j][0] = sacc2[h2][j][1] = sacc2[h2][j][2] = sacc2[h2][j][3] = 0.0f;
         const uint32_t a_addr = q_a + (mt_s * 16 + (lane & 15)) * kRowB + (lane >> 4) * 16;
-#pragma unroll 4
+        const uint32_t b_addr =
+            NTW == 2 ? kv_a + (n_s0 + (lane & 7) + ((lane >> 4) << 3)) * kRowB + ((lane >> 3) & 1) * 16
+                     : kv_a + (n_s0 + (lane & 7)) * kRowB + ((lane >> 3) & 1) * 16;
+        uint32_t fa[2][4], fb[2][4];
+        auto load_step = [&](int kk, int sl) {
+          ldsm_x4(a_addr + kk * 32, fa[sl][0], fa[sl][1], fa[sl][2], fa[sl][3]);
+          if (NTW == 2)
+            ldsm_x4(b_addr + kk * 32, fb[sl][0], fb[sl][1], fb[sl][2], fb[sl][3]);
+          else
+            ldsm_x2(b_addr + kk * 32, fb[sl][0], fb[sl][1]);
+        };
+        load_step(0, 0);
+#pragma unroll
         for (int kk = 0; kk < kKvDim / 16; ++kk) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(a_addr + kk * 32, a0, a1, a2, a3);
-          if (NTW == 2) {
-            uint32_t b0, b1, b2, b3;
-            const int trow = n_s0 + (lane & 7) + ((lane >> 4) << 3);
-            ldsm_x4(kv_a + trow * kRowB + kk * 32 + ((lane >> 3) & 1) * 16, b0, b1, b2, b3);
-            mma16816<kFp8>(sacc[0], a0, a1, a2, a3, b0, b1);
-            mma16816<kFp8>(sacc[NTW - 1], a0, a1, a2, a3, b2, b3);
-          } else {
-            uint32_t b0, b1;
-            const int trow = n_s0 + (lane & 7);
-            ldsm_x2(kv_a + trow * kRowB + kk * 32 + ((lane >> 3) & 1) * 16, b0, b1);
-            mma16816<kFp8>(sacc[0], a0, a1, a2, a3, b0, b1);
-          }
+          const int sl = kk & 1;
+          if (kk + 1 < kKvDim / 16) load_step(kk + 1, sl ^ 1);
+          mma16816<kFp8>(sacc2[sl][0], fa[sl][0], fa[sl][1], fa[sl][2], fa[sl][3], fb[sl][0], fb[sl][1]);
+          if (NTW == 2)
+            mma16816<kFp8>(sacc2[sl][NTW - 1], fa[sl][0], fa[sl][1], fa[sl][2], fa[sl][3], fb[sl][2],
+                           fb[sl][3]);
         }
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) sacc[j][c] = sacc2[0][j][c] + sacc2[1][j][c];
       }
       // logits in base 2, masked past the split's end
       float mx0 = -__int_as_float(0x7f800000), mx1 = mx0;
@@ -455,33 +495,50 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
           o[a][j][3] *= alpha[a][1];
         }
       {
-        const uint32_t p_a = smem_u32(p_s);
-        const int d0 = warp * 64;
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          uint32_t af[MT][4], al[MT][4];
+        // 16 steps (4 token slices x 4 pairs of 8-dim column tiles), each
+        // step's fragments requested one step ahead; the hi terms of P issue
+        // before the lo terms so that no MMA waits for its accumulator
+        const uint32_t p_a = smem_u32(p_s) + (lane & 15) * kPRowB + (lane >> 4) * 16;
+        const uint32_t v_a =
+            kv_a + ((lane & 7) + ((lane >> 3) & 1) * 8) * kRowB + (warp * 64 + (lane >> 4) * 8) * 2;
+        uint32_t af[2][MT][4], al[2][MT][4], bv[2][4];
+        auto load_p = [&](int kk, int sl) {
 #pragma unroll
           for (int a = 0; a < MT; ++a) {
-            ldsm_x4(p_a + (a * 16 + (lane & 15)) * kPRowB + kk * 32 + (lane >> 4) * 16, af[a][0],
-                    af[a][1], af[a][2], af[a][3]);
+            ldsm_x4(p_a + a * 16 * kPRowB + kk * 32, af[sl][a][0], af[sl][a][1], af[sl][a][2],
+                    af[sl][a][3]);
             if (!kFp8)
-              ldsm_x4(p_a + (H + a * 16 + (lane & 15)) * kPRowB + kk * 32 + (lane >> 4) * 16,
-                      al[a][0], al[a][1], al[a][2], al[a][3]);
+              ldsm_x4(p_a + (H + a * 16) * kPRowB + kk * 32, al[sl][a][0], al[sl][a][1],
+                      al[sl][a][2], al[sl][a][3]);
+          }
+        };
+        auto load_v = [&](int st, int sl) {
+          const int kk = st >> 2, jp = st & 3;
+          ldsm_x4_t(v_a + kk * 16 * kRowB + jp * 32, bv[sl][0], bv[sl][1], bv[sl][2], bv[sl][3]);
+        };
+        load_p(0, 0);
+        load_v(0, 0);
+#pragma unroll
+        for (int st = 0; st < (kTile / 16) * 4; ++st) {
+          const int kk = st >> 2, j = (st & 3) * 2, sv = st & 1, sp = kk & 1;
+          if (st + 1 < (kTile / 16) * 4) {
+            if (((st + 1) & 3) == 0) load_p(kk + 1, sp ^ 1);
+            load_v(st + 1, sv ^ 1);
           }
 #pragma unroll
-          for (int j = 0; j < 8; j += 2) {
-            uint32_t b0, b1, b2, b3;
-            const int trow = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int dcol = d0 + (j + (lane >> 4)) * 8;
-            ldsm_x4_t(kv_a + trow * kRowB + dcol * 2, b0, b1, b2, b3);
+          for (int a = 0; a < MT; ++a) {
+            mma16816<kFp8>(o[a][j], af[sp][a][0], af[sp][a][1], af[sp][a][2], af[sp][a][3],
+                           bv[sv][0], bv[sv][1]);
+            mma16816<kFp8>(o[a][j + 1], af[sp][a][0], af[sp][a][1], af[sp][a][2], af[sp][a][3],
+                           bv[sv][2], bv[sv][3]);
+          }
+          if (!kFp8) {
 #pragma unroll
             for (int a = 0; a < MT; ++a) {
-              mma16816<kFp8>(o[a][j], af[a][0], af[a][1], af[a][2], af[a][3], b0, b1);
-              mma16816<kFp8>(o[a][j + 1], af[a][0], af[a][1], af[a][2], af[a][3], b2, b3);
-              if (!kFp8) {
-                mma16816<false>(o[a][j], al[a][0], al[a][1], al[a][2], al[a][3], b0, b1);
-                mma16816<false>(o[a][j + 1], al[a][0], al[a][1], al[a][2], al[a][3], b2, b3);
-              }
+              mma16816<false>(o[a][j], al[sp][a][0], al[sp][a][1], al[sp][a][2], al[sp][a][3],
+                              bv[sv][0], bv[sv][1]);
+              mma16816<false>(o[a][j + 1], al[sp][a][0], al[sp][a][1], al[sp][a][2],
+                              al[sp][a][3], bv[sv][2], bv[sv][3]);
             }
           }
         }

@@ -4,20 +4,26 @@
 // Motivation: DSA keeps the top 2048 tokens of the whole sequence; Modifications
 // / Indexer decode: every shard first keeps a local top-k of its own tokens.
 //
-// One cluster of kCluster CTAs (1024 threads each) per score row; CTA c owns
-// the c-th contiguous segment of the row:
-//   1. its scores become order-preserving uint32 keys (-0 == +0), cached in
-//      shared memory when the segment fits; the same pass builds the segment's
-//      histogram of the top 13 key bits;
-//   2. every CTA sums the cluster's histograms through distributed shared
-//      memory and finds the bin holding the k-th largest key; two more
-//      histograms (10 and 9 bits) over only the keys still in play refine it
-//      to the exact threshold key T and how many keys equal to T are taken
-//      (the lowest positions win ties);
-//   3. an order-preserving compaction writes the selected positions in
-//      ascending order: each CTA learns from the others' counts where its
-//      segment's selections start, then every warp owns a contiguous piece of
-//      the segment and writes its selected positions at their final slots.
+// A cluster of C CTAs (1024 threads each; C = 4, 2 or 1, the most that keeps
+// every row's cluster resident at once) per score row; CTA c owns the c-th
+// contiguous segment of the row:
+//   1. the segment's scores become order-preserving uint32 keys (-0 == +0),
+//      cached in shared memory as far as they fit; the row's smallest and
+//      largest keys bound the bits in which keys differ;
+//   2. one histogram of the top 11 of those bits (summed over the cluster
+//      through distributed shared memory) gives the bin b1 holding the k-th
+//      largest key.  Keys above b1 are selected for sure; one classifying pass
+//      counts them per warp and lists the few keys inside b1 (the candidates,
+//      with their positions) in shared memory;
+//   3. every CTA reads the cluster's candidates and resolves the remaining
+//      bits on them alone: the exact threshold key T and how many keys equal
+//      to T are taken (the lowest positions win ties).  A degenerate row whose
+//      b1 holds too many keys instead resolves them with more histogram
+//      rounds over the whole row;
+//   4. an order-preserving compaction writes the selected positions in
+//      ascending order: from the per-warp counts every warp knows its first
+//      output slot, and writes 128 keys' selections per step (4 per lane,
+//      warp scans for the slots).
 // No sort: the list comes out in position order.
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
@@ -28,35 +34,57 @@ namespace {
 
 constexpr int kThreads = kSelThreads;
 constexpr int kWarps = kThreads / 32;
-constexpr int kCluster = 4;  // CTAs per score row
+constexpr int kRoundBits = 11;          // key bits resolved per histogram round
+constexpr int kBins = 1 << kRoundBits;
+constexpr int kCand = 4096;             // candidates of a row (cluster-wide)
 constexpr int kSmemLimit = 227 * 1024;
-constexpr int kBins1 = kSelBins1;
-constexpr int kShift1 = kSelShift1;
+
+// misc words
+constexpr int kSh = 32;        // [32] shared scalars
+constexpr int kWgt = 64;       // [32] per warp: keys above T
+constexpr int kWeq = 96;       // [32] per warp: keys equal to T
+constexpr int kWdef = 128;     // [32] per warp: keys above the bin b1
+constexpr int kPub = 160;      // [16] read by the cluster: min, max, candidates, keys above b1
+constexpr int kTmp = 192;      // [64] reductions
+constexpr int kCtaCnt = 256;   // [8] per CTA of the cluster: keys above T, keys equal to T
+constexpr int kMiscWords = 512;
 
 struct TopkSmem {
   int cap;         // keys of the CTA's segment cached in smem
-  int off_hist, off_red, off_misc, off_keys, total;
+  int off_hist, off_red, off_misc, off_cand, off_all, off_keys, total;
 };
 
-__host__ inline TopkSmem topk_smem() {
+__host__ inline TopkSmem topk_smem(int C) {
   TopkSmem s{};
-  s.off_hist = 0;                       // this CTA's histogram (read by the cluster)
-  s.off_red = s.off_hist + kBins1 * 4;  // the cluster's summed histogram
-  s.off_misc = s.off_red + kBins1 * 4;
-  s.off_keys = s.off_misc + 1024;
-  s.cap = ((kSmemLimit - s.off_keys) / 4) & ~1023;
+  s.off_hist = 0;                                  // this CTA's histogram (read by the cluster)
+  s.off_red = s.off_hist + kBins * 4;              // the cluster's summed histogram
+  s.off_misc = s.off_red + (C > 1 ? kBins * 4 : 0);
+  s.off_cand = s.off_misc + kMiscWords * 4;        // this CTA's candidates (key, position)
+  s.off_all = s.off_cand + kCand * 8;              // the cluster's candidates
+  s.off_keys = s.off_all + (C > 1 ? kCand * 8 : 0);
+  s.cap = ((kSmemLimit - s.off_keys) / 4) & ~127;
   s.total = s.off_keys + s.cap * 4;
   return s;
 }
 
-// red[b] = sum over the cluster's CTAs of hist[b], b < nb (nb a multiple of
-// 4 * kThreads or smaller than it, and of 4)
+// inclusive prefix sum over the lanes of a warp
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// red[b] = sum over the cluster's CTAs of hist[b], b < nb (nb a multiple of 4)
+template <int C>
 __device__ __forceinline__ void cluster_sum_hist(const uint32_t* hist, uint32_t* red, int nb) {
   const uint32_t base = smem_u32(hist);
   for (int v = threadIdx.x; v < nb / 4; v += kThreads) {
     uint4 acc = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-    for (int c = 0; c < kCluster; ++c) {
+    for (int c = 0; c < C; ++c) {
       const uint4 x = dsmem_ld_v4(dsmem_map(base + v * 16, c));
       acc.x += x.x;
       acc.y += x.y;
@@ -68,24 +96,91 @@ __device__ __forceinline__ void cluster_sum_hist(const uint32_t* hist, uint32_t*
   __syncthreads();
 }
 
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
+// sum of v over the lanes at and above this one
+__device__ __forceinline__ uint32_t warp_suffix_incl(uint32_t v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xffffffffu, v, o);
+    if (lane + o < 32) v += t;
+  }
+  return v;
+}
+
+// One warp: the bin of hist[0, nb) (nb a power of two up to 2048; a higher
+// bin holds larger keys) that holds the k_rem-th largest key.  Lane 0 writes
+// (bin, k_rem within the bin, the bin's count) to out[0..2].  Two levels:
+// every lane sums a contiguous run of nb / 32 bins, a suffix scan finds the
+// run, and the run's bins are spread over the lanes for a second scan.
+__device__ void warp_find_bin(const uint32_t* hist, int nb, uint32_t k_rem, uint32_t* out,
+                              int lane) {
+  const int per = nb >= 32 ? nb / 32 : 1;
+  const int base = lane * per;
+  uint32_t mine = 0;
+  if (base < nb) {
+    if (per >= 4) {
+      for (int j = 0; j < per; j += 4) {
+        const uint4 x = *reinterpret_cast<const uint4*>(hist + base + j);
+        mine += x.x + x.y + x.z + x.w;
+      }
+    } else {
+      for (int j = 0; j < per; ++j) mine += hist[base + j];
+    }
+  }
+  const uint32_t incl = warp_suffix_incl(mine, lane);
+  const uint32_t above = incl - mine;
+  const unsigned hit = __ballot_sync(0xffffffffu, base < nb && above < k_rem && incl >= k_rem);
+  const int fl = hit ? __ffs(hit) - 1 : 0;
+  const uint32_t abv = __shfl_sync(0xffffffffu, above, fl);
+  // the found run, per2 bins per lane
+  const int per2 = per >= 32 ? per / 32 : 1;
+  const int b0 = fl * per + lane * per2;
+  const bool in2 = lane * per2 < per;
+  uint32_t m2 = 0;
+  if (in2)
+    for (int j = 0; j < per2; ++j) m2 += hist[b0 + j];
+  const uint32_t incl2 = warp_suffix_incl(m2, lane) + abv;
+  const uint32_t above2 = incl2 - m2;
+  const unsigned hit2 = __ballot_sync(0xffffffffu, in2 && above2 < k_rem && incl2 >= k_rem);
+  const int fl2 = hit2 ? __ffs(hit2) - 1 : 0;
+  if (lane == fl2) {
+    uint32_t acc = above2;
+    for (int j = per2 - 1; j >= 0; --j) {
+      const uint32_t h = hist[b0 + j];
+      if (acc + h >= k_rem || j == 0) {
+        out[0] = static_cast<uint32_t>(b0 + j);
+        out[1] = k_rem - acc;
+        out[2] = h;
+        break;
+      }
+      acc += h;
+    }
+  }
+  __syncwarp();
+}
+
+template <int C>
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
     topk_kernel(const TopkLaunch P, const TopkSmem S) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + S.off_hist);
-  uint32_t* red = reinterpret_cast<uint32_t*>(smem + S.off_red);
+  uint32_t* red = C > 1 ? reinterpret_cast<uint32_t*>(smem + S.off_red) : hist;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + S.off_misc);
+  uint2* cand = reinterpret_cast<uint2*>(smem + S.off_cand);
+  uint2* cand_all = C > 1 ? reinterpret_cast<uint2*>(smem + S.off_all) : cand;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + S.off_keys);
-  uint32_t* scratch = misc;       // 32 words
-  uint32_t* sh = misc + 64;       // shared scalars
-  uint32_t* cnt = misc + 96;      // [2] this CTA's keys above / equal to T (read by the cluster)
-  uint32_t* wgt = misc + 128;     // [32] keys above T per warp
-  uint32_t* weq = misc + 160;     // [32] keys equal to T per warp
+  uint32_t* sh = misc + kSh;
+  uint32_t* wgt = misc + kWgt;
+  uint32_t* weq = misc + kWeq;
+  uint32_t* wdef = misc + kWdef;
+  uint32_t* pub = misc + kPub;
+  uint32_t* tmp = misc + kTmp;
+  uint32_t* ctacnt = misc + kCtaCnt;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const uint32_t crank = cluster_ctarank();
-  const int q = blockIdx.x / kCluster;
+  const uint32_t crank = C > 1 ? cluster_ctarank() : 0u;
+  const int q = blockIdx.x / C;
   const int w = q / P.rows;
   const int r = q - w * P.rows;
   const int k = P.k;
@@ -104,24 +199,23 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   }
   const float* src = P.scores + static_cast<long long>(w) * P.shard_stride +
                      static_cast<long long>(r) * P.ld;
-  // this CTA's segment [c0, c1) of the row, 32-aligned starts
-  const int cseg = (((n + kCluster - 1) / kCluster) + 31) & ~31;
+  // this CTA's segment [c0, c0 + m) of the row, 32-aligned starts
+  const int cseg = C > 1 ? ((((n + C - 1) / C) + 31) & ~31) : n;
   const int c0 = min(n, static_cast<int>(crank) * cseg);
-  const int c1 = min(n, c0 + cseg);
-  const int m = c1 - c0;
-  const bool in_smem = m <= S.cap;
-  const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+  const int m = min(n, c0 + cseg) - c0;
+  const float* seg = src + c0;
+  const bool vec = (reinterpret_cast<uintptr_t>(seg) & 15u) == 0;
+  const int cached = min(m, S.cap);  // segment keys [0, cached) live in smem
   const int cnt_all = n < k ? n : k;
   const bool need_select = n > k;
 
-  for (int b = tid; b < kBins1; b += kThreads) hist[b] = 0;
-  if (tid < 16) sh[tid] = 0;
+  for (int i = tid; i < kMiscWords; i += kThreads) misc[i] = 0;
   __syncthreads();
 
-  // ---------------- pass 1: keys (+ smem copy) and the 13-bit histogram
+  // ---------------- pass 1: keys (+ smem copy), smallest and largest key
   bool nan_seen = false;
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   {
-    const float* seg = src + c0;
     const int nv = vec ? (m >> 2) : 0;
     const float4* src4 = reinterpret_cast<const float4*>(seg);
     for (int base = 0; base < nv; base += kThreads * 4) {
@@ -142,9 +236,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 4; ++e) {
             nan_seen |= (f[e] != f[e]);
             kp[e] = score_key(f[e]);
-            if (need_select) atomicAdd(hist + (kp[e] >> kShift1), 1u);
+            kmin = min(kmin, kp[e]);
+            kmax = max(kmax, kp[e]);
           }
-          if (in_smem) reinterpret_cast<uint4*>(keys)[i] = kk;
+          // cached is m or a multiple of 128: a vector lies wholly on one side
+          if (4 * i < cached) reinterpret_cast<uint4*>(keys)[i] = kk;
         }
       }
     }
@@ -152,120 +248,421 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
       const float f = __ldg(seg + i);
       nan_seen |= (f != f);
       const uint32_t key = score_key(f);
-      if (need_select) atomicAdd(hist + (key >> kShift1), 1u);
-      if (in_smem) keys[i] = key;
+      kmin = min(kmin, key);
+      kmax = max(kmax, key);
+      if (i < cached) keys[i] = key;
     }
   }
-  if (nan_seen) sh[0] = 1;
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  const bool nan_warp = __any_sync(0xffffffffu, nan_seen);
+  if (lane == 0) {
+    tmp[warp] = kmin;
+    tmp[32 + warp] = kmax;
+    if (nan_warp) sh[2] = 1;
+  }
   __syncthreads();
-  if (tid == 0 && sh[0]) raise_err(P.d_err, DSA_DEVERR_NAN);
+  if (warp == 0) {
+    const uint32_t a = __reduce_min_sync(0xffffffffu, tmp[lane]);
+    const uint32_t b = __reduce_max_sync(0xffffffffu, tmp[32 + lane]);
+    if (lane == 0) {
+      pub[0] = a;
+      pub[1] = b;
+    }
+  }
+  __syncthreads();
+  if constexpr (C > 1) {
+    cluster_sync();  // every CTA's min and max are visible to the cluster
+    if (warp == 0) {
+      uint32_t a = 0xFFFFFFFFu, b = 0u;
+      if (lane < C) {
+        a = dsmem_ld(dsmem_map(smem_u32(pub), lane));
+        b = dsmem_ld(dsmem_map(smem_u32(pub + 1), lane));
+      }
+      a = __reduce_min_sync(0xffffffffu, a);
+      b = __reduce_max_sync(0xffffffffu, b);
+      if (lane == 0) {
+        sh[0] = a;
+        sh[1] = b;
+      }
+    }
+  } else {
+    if (tid == 0) {
+      sh[0] = pub[0];
+      sh[1] = pub[1];
+    }
+  }
+  __syncthreads();
+  kmin = sh[0];
+  kmax = sh[1];
+  if (tid == 0 && sh[2]) raise_err(P.d_err, DSA_DEVERR_NAN);
 
-  // key of row position i of this CTA's segment
-  auto key_at = [&](int i) -> uint32_t {
-    return in_smem ? keys[i - c0] : score_key(__ldg(src + i));
+  // key of segment position j
+  auto key_at = [&](int j) -> uint32_t {
+    return j < cached ? keys[j] : score_key(__ldg(seg + j));
+  };
+  // the keys of segment positions j0 .. j0 + 3 below lim (j0 a multiple of 4)
+  auto load4 = [&](int j0, int lim, uint32_t* kv, bool* ok) {
+    if (j0 + 3 < lim && j0 + 3 < cached) {
+      const uint4 x = *reinterpret_cast<const uint4*>(keys + j0);
+      kv[0] = x.x;
+      kv[1] = x.y;
+      kv[2] = x.z;
+      kv[3] = x.w;
+      ok[0] = ok[1] = ok[2] = ok[3] = true;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        ok[e] = j0 + e < lim;
+        kv[e] = ok[e] ? key_at(j0 + e) : 0u;
+      }
+    }
   };
 
+  // warp pieces of the segment (segment positions), 32-aligned
+  const int wseg = ((m + kWarps - 1) / kWarps + 31) & ~31;
+  const int s0 = min(m, warp * wseg), s1 = min(m, s0 + wseg);
+
+  // mode 0: n <= k, every position; 1: threshold from the candidates;
+  // 2: threshold from rounds over the whole row (or a single key value)
+  int mode = 0;
   uint32_t T = 0, k_rem = 0;
+  uint64_t pre = 0;  // the threshold's bits above bit lo - 1
+  int lo = 0;
+  const uint32_t diff = kmin ^ kmax;
   if (need_select) {
-    // ---------------- the exact k-th largest key over the cluster's histograms
-    cluster_sync();                       // every CTA's 13-bit histogram is complete
-    cluster_sum_hist(hist, red, kBins1);
-    find_bin(red, kBins1, static_cast<uint32_t>(k), scratch, sh + 4);
-    const uint32_t b1 = sh[4];
-    k_rem = sh[5];
-    cluster_sync();                       // every CTA has read the histograms
-    for (int b = tid; b < kSelBins2; b += kThreads) hist[b] = 0;
-    __syncthreads();
-    for (int i = c0 + tid; i < c1; i += kThreads) {
-      const uint32_t key = key_at(i);
-      if ((key >> kShift1) == b1) atomicAdd(hist + ((key >> kSelShift2) & (kSelBins2 - 1)), 1u);
+    if (diff == 0) {
+      mode = 2;
+      T = kmax;  // one key value: the first k positions
+      k_rem = static_cast<uint32_t>(k);
+    } else {
+      const int top = 31 - __clz(diff);  // highest bit in which keys differ
+      const int nbits = min(kRoundBits, top + 1);
+      lo = top + 1 - nbits;
+      const int nb = 1 << nbits;
+      const int nbz = max(nb, 4);
+      for (int b = tid; b < nbz; b += kThreads) hist[b] = 0;
+      __syncthreads();
+      const uint32_t bmask = static_cast<uint32_t>(nb - 1);
+      for (int j4 = tid; j4 < (cached >> 2); j4 += kThreads) {
+        const uint4 x = reinterpret_cast<const uint4*>(keys)[j4];
+        atomicAdd(hist + ((x.x >> lo) & bmask), 1u);
+        atomicAdd(hist + ((x.y >> lo) & bmask), 1u);
+        atomicAdd(hist + ((x.z >> lo) & bmask), 1u);
+        atomicAdd(hist + ((x.w >> lo) & bmask), 1u);
+      }
+      for (int j = (cached & ~3) + tid; j < m; j += kThreads)
+        atomicAdd(hist + ((key_at(j) >> lo) & bmask), 1u);
+      __syncthreads();
+      if constexpr (C > 1) {
+        cluster_sync();  // every CTA's histogram is complete
+        cluster_sum_hist<C>(hist, red, nbz);
+      }
+      if (warp == 0) warp_find_bin(red, nb, static_cast<uint32_t>(k), sh + 4, lane);
+      __syncthreads();
+      pre = ((static_cast<uint64_t>(kmax) >> (top + 1)) << nbits) | sh[4];
+      k_rem = sh[5];
+      mode = sh[6] <= static_cast<uint32_t>(kCand) ? 1 : 2;
     }
-    cluster_sync();
-    cluster_sum_hist(hist, red, kSelBins2);
-    find_bin(red, kSelBins2, k_rem, scratch, sh + 4);
-    const uint32_t pre2 = (b1 << (kShift1 - kSelShift2)) | sh[4];
-    k_rem = sh[5];
-    cluster_sync();
-    for (int b = tid; b < kSelBins3; b += kThreads) hist[b] = 0;
-    __syncthreads();
-    for (int i = c0 + tid; i < c1; i += kThreads) {
-      const uint32_t key = key_at(i);
-      if ((key >> kSelShift2) == pre2) atomicAdd(hist + (key & (kSelBins3 - 1)), 1u);
-    }
-    cluster_sync();
-    cluster_sum_hist(hist, red, kSelBins3);
-    find_bin(red, kSelBins3, k_rem, scratch, sh + 4);
-    T = (pre2 << kSelShift2) | sh[4];
-    k_rem = sh[5];  // keys equal to T that are taken (the lowest positions)
   }
+
+  if (mode == 1) {
+    // ---------------- classify: keys above b1 per warp, candidates listed
+    uint32_t ndef = 0;
+    for (int s = s0; s < s1; s += 128) {
+      const int j0 = s + 4 * lane;
+      uint32_t kv[4];
+      bool ok[4];
+      load4(j0, s1, kv, ok);
+      uint32_t nc = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint64_t hi = kv[e] >> lo;
+        ndef += (ok[e] && hi > pre) ? 1u : 0u;
+        nc += (ok[e] && hi == pre) ? 1u : 0u;
+      }
+      const uint32_t incl = warp_incl_scan(nc, lane);
+      const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+      if (tot != 0) {
+        uint32_t base = 0;
+        if (lane == 31) base = atomicAdd(sh + 8, tot);
+        base = __shfl_sync(0xffffffffu, base, 31);
+        uint32_t slot = base + incl - nc;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (ok[e] && (static_cast<uint64_t>(kv[e] >> lo) == pre)) {
+            cand[slot] = make_uint2(kv[e], static_cast<uint32_t>(c0 + j0 + e));
+            ++slot;
+          }
+        }
+      }
+    }
+    ndef = __reduce_add_sync(0xffffffffu, ndef);
+    if (lane == 0) wdef[warp] = ndef;
+    __syncthreads();
+    const uint32_t nloc = sh[8];
+    uint32_t total = nloc;
+    if constexpr (C > 1) {
+      if (warp == 0) {
+        const uint32_t d = __reduce_add_sync(0xffffffffu, wdef[lane]);
+        if (lane == 0) {
+          pub[2] = nloc;
+          pub[3] = d;
+        }
+      }
+      __syncthreads();
+      // every CTA's candidates and counts are visible, and every CTA is done
+      // reading the others' histograms
+      cluster_sync();
+      if (warp == 0) {
+        uint32_t nc = 0, d = 0;
+        if (lane < C) {
+          nc = dsmem_ld(dsmem_map(smem_u32(pub + 2), lane));
+          d = dsmem_ld(dsmem_map(smem_u32(pub + 3), lane));
+        }
+        const uint32_t incl = warp_incl_scan(nc, lane);
+        if (lane < C) {
+          tmp[lane] = incl - nc;
+          tmp[8 + lane] = nc;
+          tmp[16 + lane] = d;
+        }
+        if (lane == 31) sh[9] = incl;
+      }
+      __syncthreads();
+      total = sh[9];
+      for (int c = 0; c < C; ++c) {
+        const uint32_t nc = tmp[8 + c], o = tmp[c];
+        for (uint32_t e = tid; e < nc; e += kThreads) {
+          const uint32_t ca = dsmem_map(smem_u32(cand + e), c);
+          cand_all[o + e] = make_uint2(dsmem_ld(ca), dsmem_ld(ca + 4));
+        }
+      }
+      __syncthreads();
+    }
+    // ---------------- the remaining bits of T, from the candidates alone
+    if (total <= static_cast<uint32_t>(kThreads)) {
+      // rank every candidate among them: T is the key with fewer than k_rem
+      // candidates above it and at least k_rem at or above it
+      if (static_cast<uint32_t>(tid) < total) {
+        const uint32_t key = cand_all[tid].x;
+        uint32_t gt = 0, eq = 0;
+#pragma unroll 4
+        for (uint32_t j = 0; j < total; ++j) {
+          const uint32_t kj = cand_all[j].x;
+          gt += kj > key ? 1u : 0u;
+          eq += kj == key ? 1u : 0u;
+        }
+        if (gt < k_rem && k_rem <= gt + eq) {
+          sh[12] = key;  // every writer writes the same two words
+          sh[13] = k_rem - gt;
+        }
+      }
+    } else if (warp == 0) {
+      // histogram rounds (warp 0; the histogram is free: every CTA is past
+      // its cluster sum)
+      int t = lo - 1;
+      while (t >= 0) {
+        const int nbits = min(kRoundBits, t + 1);
+        const int lo2 = t + 1 - nbits;
+        const int nb = 1 << nbits;
+        for (int b = lane; b < nb; b += 32) hist[b] = 0;
+        __syncwarp();
+        for (uint32_t e = lane; e < total; e += 32) {
+          const uint32_t key = cand_all[e].x;
+          if (static_cast<uint64_t>(key >> (t + 1)) == pre)
+            atomicAdd(hist + ((key >> lo2) & static_cast<uint32_t>(nb - 1)), 1u);
+        }
+        __syncwarp();
+        warp_find_bin(hist, nb, k_rem, sh + 4, lane);
+        pre = (pre << nbits) | sh[4];
+        k_rem = sh[5];
+        __syncwarp();
+        t = lo2 - 1;
+      }
+      if (lane == 0) {
+        sh[12] = static_cast<uint32_t>(pre);
+        sh[13] = k_rem;
+      }
+    }
+    __syncthreads();
+    T = sh[12];
+    k_rem = sh[13];
+    // candidates above / equal to T, per warp of this CTA and per CTA
+    for (uint32_t e = tid; e < nloc; e += kThreads) {
+      const uint2 c = cand[e];
+      const int wj = (static_cast<int>(c.y) - c0) / wseg;
+      if (c.x > T) atomicAdd(wgt + wj, 1u);
+      else if (c.x == T) atomicAdd(weq + wj, 1u);
+    }
+    if constexpr (C > 1) {
+      for (uint32_t e = tid; e < total; e += kThreads) {
+        const uint2 c = cand_all[e];
+        const int cc = static_cast<int>(c.y) / cseg;
+        if (c.x > T) atomicAdd(ctacnt + 2 * cc, 1u);
+        else if (c.x == T) atomicAdd(ctacnt + 2 * cc + 1, 1u);
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t g = 0, eqb = 0;
+      if constexpr (C > 1) {
+        for (uint32_t c = 0; c < crank; ++c) {
+          g += tmp[16 + c] + ctacnt[2 * c];
+          eqb += ctacnt[2 * c + 1];
+        }
+      }
+      sh[10] = g;
+      sh[11] = eqb;
+    }
+  } else if (mode == 2) {
+    // ---------------- degenerate rows: rounds over the whole row
+    while (diff != 0 && lo > 0) {
+      if constexpr (C > 1) cluster_sync();  // every CTA is done reading the histograms
+      const int t = lo - 1;
+      const int nbits = min(kRoundBits, t + 1);
+      const int lo2 = t + 1 - nbits;
+      const int nb = 1 << nbits;
+      const int nbz = max(nb, 4);
+      for (int b = tid; b < nbz; b += kThreads) hist[b] = 0;
+      __syncthreads();
+      for (int j = tid; j < m; j += kThreads) {
+        const uint32_t key = key_at(j);
+        if (static_cast<uint64_t>(key >> (t + 1)) == pre)
+          atomicAdd(hist + ((key >> lo2) & static_cast<uint32_t>(nb - 1)), 1u);
+      }
+      __syncthreads();
+      if constexpr (C > 1) {
+        cluster_sync();
+        cluster_sum_hist<C>(hist, red, nbz);
+      }
+      if (warp == 0) warp_find_bin(red, nb, k_rem, sh + 4, lane);
+      __syncthreads();
+      pre = (pre << nbits) | sh[4];
+      k_rem = sh[5];
+      lo = lo2;
+      __syncthreads();  // sh is read before the next round writes it
+    }
+    if (diff != 0) T = static_cast<uint32_t>(pre);
+    // keys above / equal to T per warp
+    uint32_t cg = 0, ce = 0;
+    for (int s = s0; s < s1; s += 128) {
+      uint32_t kv[4];
+      bool ok[4];
+      load4(s + 4 * lane, s1, kv, ok);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        cg += (ok[e] && kv[e] > T) ? 1u : 0u;
+        ce += (ok[e] && kv[e] == T) ? 1u : 0u;
+      }
+    }
+    cg = __reduce_add_sync(0xffffffffu, cg);
+    ce = __reduce_add_sync(0xffffffffu, ce);
+    if (lane == 0) {
+      wgt[warp] = cg;
+      weq[warp] = ce;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t g = 0, e = 0;
+      for (int v = 0; v < kWarps; ++v) {
+        g += wgt[v];
+        e += weq[v];
+      }
+      pub[4] = g;
+      pub[5] = e;
+    }
+    __syncthreads();
+    if constexpr (C > 1) cluster_sync();  // every CTA's counts are visible
+    if (warp == 0) {
+      uint32_t g = 0, e = 0;
+      if constexpr (C > 1) {
+        if (static_cast<uint32_t>(lane) < crank) {
+          g = dsmem_ld(dsmem_map(smem_u32(pub + 4), lane));
+          e = dsmem_ld(dsmem_map(smem_u32(pub + 5), lane));
+        }
+      }
+      g = __reduce_add_sync(0xffffffffu, g);
+      e = __reduce_add_sync(0xffffffffu, e);
+      if (lane == 0) {
+        sh[10] = g;
+        sh[11] = e;
+      }
+    }
+  } else {
+    if (tid == 0) {
+      sh[10] = static_cast<uint32_t>(c0);  // every position before the segment
+      sh[11] = 0;
+    }
+  }
+  __syncthreads();
+  // sh[10], sh[11]: keys above T and keys equal to T in the CTAs before this
+  // one.  Ties are taken in position order, so the ties taken before any
+  // point are min(ties before it, k_rem).
 
   // ---------------- order-preserving compaction
   const int off = P.index_offset + (P.offset_per_shard ? (w + P.shard_offset) : 0);
   int32_t* oi = P.out_idx + static_cast<long long>(q) * k;
   float* os = P.out_score ? P.out_score + static_cast<long long>(q) * k : nullptr;
-  const bool all = !need_select;  // n <= k: every position is selected
-  const int wseg = ((m + kWarps - 1) / kWarps + 31) & ~31;
-  const int s0 = min(c1, c0 + warp * wseg), s1 = min(c1, s0 + wseg);
+  const bool all = mode == 0;
+  uint32_t sel_before, eq_before;
   {
-    uint32_t cg = 0, ce = 0;
-    if (!all) {
-      for (int i0 = s0; i0 < s1; i0 += 32) {
-        const int i = i0 + lane;
-        const uint32_t key = i < s1 ? key_at(i) : 0u;
-        cg += __popc(__ballot_sync(0xffffffffu, i < s1 && key > T));
-        ce += __popc(__ballot_sync(0xffffffffu, i < s1 && key == T));
+    const int v0 = min(m, lane * wseg);
+    const uint32_t g = all ? static_cast<uint32_t>(min(m, v0 + wseg) - v0) : wdef[lane] + wgt[lane];
+    const uint32_t e = weq[lane];
+    const uint32_t gi = warp_incl_scan(g, lane), ei = warp_incl_scan(e, lane);
+    // this warp's exclusive prefix over the warps before it
+    const uint32_t gx = __shfl_sync(0xffffffffu, gi - g, warp);
+    const uint32_t ex = __shfl_sync(0xffffffffu, ei - e, warp);
+    eq_before = sh[11] + ex;
+    sel_before = sh[10] + gx + min(eq_before, k_rem);
+  }
+  for (int s = s0; s < s1; s += 128) {
+    const int j0 = s + 4 * lane;
+    uint32_t kv[4];
+    bool ok[4];
+    if (all) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        ok[e] = j0 + e < s1;
+        kv[e] = 0u;
       }
     } else {
-      cg = static_cast<uint32_t>(s1 - s0);
+      load4(j0, s1, kv, ok);
     }
-    if (lane == 0) {
-      wgt[warp] = cg;
-      weq[warp] = ce;
+    bool eqf[4];
+    uint32_t neq = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      eqf[e] = ok[e] && !all && kv[e] == T;
+      neq += eqf[e] ? 1u : 0u;
     }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t g = 0, e = 0;
-    for (int v = 0; v < kWarps; ++v) {
-      g += wgt[v];
-      e += weq[v];
+    const uint32_t eincl = warp_incl_scan(neq, lane);
+    uint32_t er = eq_before + eincl - neq;  // rank of this lane's first tie
+    bool self[4];
+    uint32_t nsel = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (eqf[e]) {
+        self[e] = er < k_rem;
+        ++er;
+      } else {
+        self[e] = ok[e] && (all || kv[e] > T);
+      }
+      nsel += self[e] ? 1u : 0u;
     }
-    cnt[0] = g;
-    cnt[1] = e;
-  }
-  cluster_sync();  // every CTA's counts are visible to the cluster
-  // selections and ties of the segments before this one (lower positions)
-  uint32_t eq_before = 0, sel_before = 0;
-  for (uint32_t c = 0; c < crank; ++c) {
-    const uint32_t g = dsmem_ld(dsmem_map(smem_u32(cnt), c));
-    const uint32_t e = dsmem_ld(dsmem_map(smem_u32(cnt + 1), c));
-    const uint32_t take = eq_before >= k_rem ? 0u : min(e, k_rem - eq_before);
-    sel_before += g + take;
-    eq_before += e;
-  }
-  for (int v = 0; v < warp; ++v) {
-    const uint32_t e = weq[v];
-    const uint32_t take = eq_before >= k_rem ? 0u : min(e, k_rem - eq_before);
-    sel_before += wgt[v] + take;
-    eq_before += e;
-  }
-  for (int i0 = s0; i0 < s1; i0 += 32) {
-    const int i = i0 + lane;
-    const bool in = i < s1;
-    const uint32_t key = (in && !all) ? key_at(i) : 0u;
-    const bool gt = in && (all || key > T);
-    const bool eq = in && !all && key == T;
-    const unsigned me = __ballot_sync(0xffffffffu, eq);
-    const uint32_t eq_rank = eq_before + __popc(me & ((1u << lane) - 1u));
-    const bool sel = gt || (eq && eq_rank < k_rem);
-    const unsigned ms = __ballot_sync(0xffffffffu, sel);
-    if (sel) {
-      const uint32_t slot = sel_before + __popc(ms & ((1u << lane) - 1u));
-      oi[slot] = i * P.index_stride + off;
-      if (os) os[slot] = all ? __ldg(src + i) : key_score(key);
+    const uint32_t sincl = warp_incl_scan(nsel, lane);
+    uint32_t slot = sel_before + sincl - nsel;  // selections before this lane's first
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (self[e]) {
+        const int pos = c0 + j0 + e;
+        oi[slot] = pos * P.index_stride + off;
+        if (os) os[slot] = all ? __ldg(seg + j0 + e) : key_score(kv[e]);
+        ++slot;
+      }
     }
-    eq_before += __popc(me);
-    sel_before += __popc(ms);
+    eq_before += __shfl_sync(0xffffffffu, eincl, 31);
+    sel_before += __shfl_sync(0xffffffffu, sincl, 31);
   }
   if (crank == 0) {
     for (int i = cnt_all + tid; i < k; i += kThreads) {
@@ -274,20 +671,29 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) P.out_count[q] = cnt_all;
   }
-  cluster_sync();  // no CTA leaves while another may still read its counts
+  if constexpr (C > 1) cluster_sync();  // no CTA leaves while another may still read its smem
+}
+
+template <int C>
+cudaError_t launch_c(const TopkLaunch& p, int rows, cudaStream_t stream) {
+  const TopkSmem S = topk_smem(C);
+  cudaError_t e =
+      cudaFuncSetAttribute(topk_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, S.total);
+  if (e != cudaSuccess) return e;
+  topk_kernel<C><<<rows * C, kThreads, S.total, stream>>>(p, S);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const TopkLaunch& p, cudaStream_t stream) {
-  const TopkSmem S = topk_smem();
-  cudaError_t e =
-      cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S.total);
-  if (e != cudaSuccess) return e;
   const int rows = p.nshards * p.rows;
   if (rows == 0) return cudaSuccess;
-  topk_kernel<<<rows * kCluster, kThreads, S.total, stream>>>(p, S);
-  return cudaGetLastError();
+  // the widest cluster that still runs every row at once (one CTA per SM)
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  if (rows * 4 <= sms) return launch_c<4>(p, rows, stream);
+  if (rows * 2 <= sms) return launch_c<2>(p, rows, stream);
+  return launch_c<1>(p, rows, stream);
 }
 
 }  // namespace dsa

@@ -86,6 +86,47 @@ def test_topk_random_rows():
     assert _topk_case(s, valid, 2048) == 0
 
 
+def test_topk_wide_and_narrow_key_ranges():
+    """Rows whose keys span many octaves, a very narrow band, a few huge
+    outliers over a narrow band, and negatives; lengths on both sides of the
+    row length whose keys still fit in shared memory."""
+    rng = np.random.default_rng(2)
+    R, L = 5, 60000
+    s = np.empty((R, L), dtype=np.float32)
+    s[0] = np.exp(rng.normal(0.0, 8.0, L))
+    s[1] = 20.0 + rng.normal(0.0, 1e-3, L)
+    s[2] = 20.0 + rng.normal(0.0, 1e-3, L)
+    s[2, ::997] = 1e30
+    s[3] = -np.exp(rng.normal(0.0, 3.0, L))
+    s[4] = rng.standard_normal(L)
+    valid = np.array([L, 55296, 55297, 40000, 2049])
+    assert _topk_case(s, valid, 2048) == 0
+    assert _topk_case(s, valid, 37) == 0
+
+
+@pytest.mark.parametrize("R", [50, 100])
+def test_topk_cluster_widths(R):
+    """Enough rows that a row gets two CTAs (50 rows) or one (100 rows)."""
+    rng = np.random.default_rng(3)
+    L = 40000
+    s = (rng.standard_normal((R, L)) * 2 + 10).astype(np.float32)
+    valid = rng.integers(1, L + 1, R)
+    valid[:4] = [L, 2048, 2049, 1]
+    assert _topk_case(s, valid, 2048) == 0
+
+
+def test_topk_crowded_threshold_bin():
+    """Three score values over 30000 positions: the bin holding the k-th
+    largest key has about 10000 keys, more than the candidate list holds."""
+    rng = np.random.default_rng(4)
+    R, L = 3, 30000
+    s = rng.integers(0, 3, (R, L)).astype(np.float32)
+    s[2] = np.where(rng.random(L) < 0.5, 7.0, 7.000001)
+    valid = np.array([L, L, L])
+    assert _topk_case(s, valid, 2048) == 0
+    assert _topk_case(s, valid, 4096) == 0
+
+
 def test_topk_ties_and_signed_zero():
     rng = np.random.default_rng(1)
     R, L = 5, 9000
