@@ -405,6 +405,10 @@ int dsa_decode(const dsa_decode_desc* d, void* workspace, size_t workspace_bytes
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int W = d->num_shards, R = d->rows.num_rows, k = d->topk;
 
+  // The kernels after the indexer are programmatic dependents of the one
+  // before them: each starts launching while its predecessor runs and waits
+  // for it before touching the predecessor's outputs.  The indexer follows
+  // the caller's work and is launched plainly.
   // 1. indexer over every shard's cache, one launch
   {
     IndexerLaunch L{};
@@ -460,7 +464,7 @@ int dsa_decode(const dsa_decode_desc* d, void* workspace, size_t workspace_bytes
       L.out_count = topk_cnt;
     }
     L.d_err = d_err;
-    if (launch_topk(L, s) != cudaSuccess) return DSA_ERR_CUDA;
+    if (launch_topk(L, s, true) != cudaSuccess) return DSA_ERR_CUDA;
   }
   // 3. exact merge of the shards' candidates; owned local rows per shard
   if (W > 1) {
@@ -475,7 +479,7 @@ int dsa_decode(const dsa_decode_desc* d, void* workspace, size_t workspace_bytes
                       reinterpret_cast<int32_t*>(ws + lay.owned_local),
                       reinterpret_cast<int32_t*>(ws + lay.owned_count),
                       d_err};
-    if (launch_shard_topk_merge(L, s) != cudaSuccess) return DSA_ERR_CUDA;
+    if (launch_shard_topk_merge(L, s, true) != cudaSuccess) return DSA_ERR_CUDA;
   }
   // 4. sparse MLA over each shard's owned rows, split-K
   {
@@ -502,11 +506,11 @@ int dsa_decode(const dsa_decode_desc* d, void* workspace, size_t workspace_bytes
       L.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
     }
     L.d_err = d_err;
-    if (launch_sparse_mla(L, s) != cudaSuccess) return DSA_ERR_CUDA;
+    if (launch_sparse_mla(L, s, true) != cudaSuccess) return DSA_ERR_CUDA;
     // 5. LSE merge of the W * S partials
     if (lay.num_parts > 1 &&
         launch_lse_merge(L.part_out, L.part_lse, lay.num_parts, R, d->heads, kVDim, d->out,
-                         d->out_lse, s) != cudaSuccess)
+                         d->out_lse, s, true) != cudaSuccess)
       return DSA_ERR_CUDA;
   }
   return DSA_OK;

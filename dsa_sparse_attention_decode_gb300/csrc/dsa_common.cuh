@@ -32,6 +32,32 @@ DSA_DEV void raise_err(int32_t* d_err, int bits) {
   if (d_err != nullptr) atomicOr(d_err, bits);
 }
 
+// Programmatic dependent launch.  A kernel lets the next kernel of its stream
+// start launching once every one of its CTAs has started (the next grid's CTAs
+// then take SMs as this grid's CTAs leave), and waits for the previous grid
+// to complete, memory included, before it reads what that grid wrote or
+// writes anything itself.  Both are no-ops in a plain launch.
+DSA_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+DSA_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Host: launch `kern`, as a programmatic dependent of the stream's previous
+// kernel when `pdl` is set.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 DSA_DEV uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  pdl_trigger();
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + L.off_bar);
   // barrier indices
@@ -226,6 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(L.tmem_cols));
     tmem_relinquish();
   }
+
+  pdl_wait();  // inputs may come from the previous grid
 
   // ---- schedule: count units of every (shard, request) pair, split evenly
   const int npairs = P.nshards * P.num_reqs;

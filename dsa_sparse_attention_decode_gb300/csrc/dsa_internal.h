@@ -63,7 +63,9 @@ struct TopkLaunch {
   int32_t* out_count;
   int32_t* d_err;
 };
-cudaError_t launch_topk(const TopkLaunch& p, cudaStream_t stream);
+// pdl: launch as a programmatic dependent of the stream's previous kernel (only
+// after kernels of this library whose outputs the kernel waits for)
+cudaError_t launch_topk(const TopkLaunch& p, cudaStream_t stream, bool pdl = false);
 
 // ------------------------------------------------------------- shard merge
 
@@ -78,7 +80,8 @@ struct MergeTopkLaunch {
   int32_t* owned_count;
   int32_t* d_err;
 };
-cudaError_t launch_shard_topk_merge(const MergeTopkLaunch& p, cudaStream_t stream);
+cudaError_t launch_shard_topk_merge(const MergeTopkLaunch& p, cudaStream_t stream,
+                                   bool pdl = false);
 
 // ------------------------------------------------------------- sparse MLA
 
@@ -108,14 +111,16 @@ struct MlaLaunch {
   float* part_lse;
   int32_t* d_err;
 };
-cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream);
+// pdl: the kernel reads the query, row_start and block tables before it waits
+// for the previous grid, which therefore must not write them
+cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream, bool pdl = false);
 int auto_mla_splits(int work_rows, int k, int expected_count);
 
 // ------------------------------------------------------------- LSE merge
 
 cudaError_t launch_lse_merge(const float* O_parts, const float* lse_parts, int parts,
                              int rows, int heads, int dv, float* out, float* out_lse,
-                             cudaStream_t stream);
+                             cudaStream_t stream, bool pdl = false);
 
 int num_sms();
 

@@ -87,9 +87,11 @@ __global__ void __launch_bounds__(kMergeThreads, 1) shard_topk_merge_kernel(cons
   uint32_t* tot = misc + 80;                            // [8] per-list totals
   const int r = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5;
+  pdl_trigger();
+  pdl_wait();  // the candidate lists come from the previous grid
 
   if (tid < W) {
-    int c = P.cand_count[tid * R + r];
+    int c = __ldcg(P.cand_count + tid * R + r);
     if (c < 0 || c > k) {
       raise_err(P.d_err, DSA_DEVERR_INDEX);
       c = c < 0 ? 0 : k;
@@ -106,8 +108,8 @@ __global__ void __launch_bounds__(kMergeThreads, 1) shard_topk_merge_kernel(cons
     const int w = e / k, i = e - w * k;
     if (i < cnt[w]) {
       const long long g = (static_cast<long long>(w) * R + r) * k + i;
-      const uint32_t key = score_key(P.cand_score[g]);
-      const int p = P.cand_pos[g];
+      const uint32_t key = score_key(__ldcg(P.cand_score + g));
+      const int p = __ldcg(P.cand_pos + g);
       if (p < 0 || p % W != w) raise_err(P.d_err, DSA_DEVERR_INDEX);
       keys[e] = key;
       pos[e] = p;
@@ -191,22 +193,24 @@ __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
                                  int heads, int dv, float* __restrict__ out,
                                  float* __restrict__ out_lse) {
   const int rh = blockIdx.x;  // r * heads + h
+  pdl_trigger();
+  pdl_wait();  // the partials come from the previous grid
   const long long stride_p = static_cast<long long>(rows) * heads;
   float m = -__int_as_float(0x7f800000);
-  for (int p = 0; p < parts; ++p) m = fmaxf(m, __ldg(lse_parts + p * stride_p + rh));
+  for (int p = 0; p < parts; ++p) m = fmaxf(m, __ldcg(lse_parts + p * stride_p + rh));
   const bool empty = (m == -__int_as_float(0x7f800000));
   float den = 0.0f;
   if (!empty)
-    for (int p = 0; p < parts; ++p) den += expf(__ldg(lse_parts + p * stride_p + rh) - m);
+    for (int p = 0; p < parts; ++p) den += expf(__ldcg(lse_parts + p * stride_p + rh) - m);
   const float inv = empty ? 0.0f : 1.0f / den;
   for (int d4 = threadIdx.x; d4 < dv / 4; d4 += blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (!empty) {
       for (int p = 0; p < parts; ++p) {
-        const float l = __ldg(lse_parts + p * stride_p + rh);
+        const float l = __ldcg(lse_parts + p * stride_p + rh);
         if (l == -__int_as_float(0x7f800000)) continue;
         const float wgt = expf(l - m) * inv;
-        const float4 v = __ldg(reinterpret_cast<const float4*>(O_parts + (p * stride_p + rh) * dv) + d4);
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(O_parts + (p * stride_p + rh) * dv) + d4);
         acc.x = fmaf(wgt, v.x, acc.x);
         acc.y = fmaf(wgt, v.y, acc.y);
         acc.z = fmaf(wgt, v.z, acc.z);
@@ -222,23 +226,23 @@ __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
 
 int merge_smem_bytes(int W, int k) { return merge_smem(W, k).total; }
 
-cudaError_t launch_shard_topk_merge(const MergeTopkLaunch& p, cudaStream_t stream) {
+cudaError_t launch_shard_topk_merge(const MergeTopkLaunch& p, cudaStream_t stream, bool pdl) {
   if (p.rows == 0) return cudaSuccess;
   const int smem = merge_smem_bytes(p.W, p.k);
   cudaError_t e = cudaFuncSetAttribute(shard_topk_merge_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  shard_topk_merge_kernel<<<p.rows, kMergeThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_ex(shard_topk_merge_kernel, dim3(p.rows), dim3(kMergeThreads), smem, stream, pdl,
+                   p);
 }
 
 cudaError_t launch_lse_merge(const float* O_parts, const float* lse_parts, int parts, int rows,
-                             int heads, int dv, float* out, float* out_lse, cudaStream_t stream) {
+                             int heads, int dv, float* out, float* out_lse, cudaStream_t stream,
+                             bool pdl) {
   if (rows * heads == 0) return cudaSuccess;
   const int threads = dv / 4 >= 128 ? 128 : ((dv / 4 + 31) / 32) * 32;
-  lse_merge_kernel<<<rows * heads, threads, 0, stream>>>(O_parts, lse_parts, parts, rows, heads,
-                                                          dv, out, out_lse);
-  return cudaGetLastError();
+  return launch_ex(lse_merge_kernel, dim3(rows * heads), dim3(threads), 0, stream, pdl, O_parts,
+                   lse_parts, parts, rows, heads, dv, out, out_lse);
 }
 
 }  // namespace dsa

@@ -147,7 +147,37 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
   const int part = w * P.num_splits + split;
   const bool direct = (P.nshards * P.num_splits == 1);
 
-  int cnt = __ldg(P.count + qrow);
+  pdl_trigger();
+  // The query and the row's request are inputs that the previous grid (when
+  // this grid is its programmatic dependent) does not write: they are fetched
+  // while it finishes.  The bf16 query copy stays in flight meanwhile.
+  const uint16_t* qsrc = P.q + static_cast<long long>(r) * H * kKvDim;
+  if (!kFp8) {
+    for (int c = tid; c < H * 72; c += kThreads) {
+      const int h = c / 72, cc = c - h * 72;
+      cp_async16(smem_u32(q_s + h * kRowB + cc * 16), qsrc + h * kKvDim + cc * 8);
+    }
+    cp_async_commit();
+  }
+
+  // request of this row: the one i with row_start[i] <= r < row_start[i + 1]
+  // (row_start is non-decreasing, so at most one non-empty request matches)
+  if (tid == 0) misc[0] = -1;
+  __syncthreads();
+  for (int i = tid; i < P.num_reqs; i += kThreads) {
+    if (__ldg(P.row_start + i) <= r && r < __ldg(P.row_start + i + 1)) misc[0] = i;
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(bars + i), kGather);   // tile landed: every gather thread's copies
+      mbar_init(smem_u32(bars + 2 + i), 1);     // buffer free: one compute thread
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  pdl_wait();  // the selections come from the previous grid
+
+  int cnt = __ldcg(P.count + qrow);
   if (cnt < 0 || cnt > P.k) {
     if (tid == 0) raise_err(P.d_err, DSA_DEVERR_INDEX);
     cnt = cnt < 0 ? 0 : P.k;
@@ -163,17 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
     for (int h = tid; h < H; h += kThreads) out_l[h] = -__int_as_float(0x7f800000);
     if (direct)
       for (int i = tid; i < H * kVDim; i += kThreads) out_o[i] = 0.0f;
+    if (!kFp8) cp_async_wait<0>();  // no copy may land after the CTA leaves
     return;
-  }
-
-  // bf16 query -> smem, in flight while the positions are looked up
-  const uint16_t* qsrc = P.q + static_cast<long long>(r) * H * kKvDim;
-  if (!kFp8) {
-    for (int c = tid; c < H * 72; c += kThreads) {
-      const int h = c / 72, cc = c - h * 72;
-      cp_async16(smem_u32(q_s + h * kRowB + cc * 16), qsrc + h * kKvDim + cc * 8);
-    }
-    cp_async_commit();
   }
 
   // the split's selected positions: all loads issued before any is used
@@ -182,22 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
 #pragma unroll
   for (int j = 0; j < kMaxPerThread; ++j) {
     const int i = tid + j * kThreads;
-    tv[j] = i < ntok ? __ldg(ilist + i) : 0;
-  }
-  // request of this row: the one i with row_start[i] <= r < row_start[i + 1]
-  // (row_start is non-decreasing, so at most one non-empty request matches)
-  if (tid == 0) misc[0] = -1;
-  __syncthreads();
-  for (int i = tid; i < P.num_reqs; i += kThreads) {
-    if (__ldg(P.row_start + i) <= r && r < __ldg(P.row_start + i + 1)) misc[0] = i;
-  }
-  if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(bars + i), kGather);   // tile landed: every gather thread's copies
-      mbar_init(smem_u32(bars + 2 + i), 1);     // buffer free: one compute thread
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
+    tv[j] = i < ntok ? __ldcg(ilist + i) : 0;
   }
 
   // bf16: wait for the query copy; fp8: the query as f16 with a per-head
@@ -586,14 +592,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
 }
 
 template <int H, bool F>
-cudaError_t launch_one(const MlaLaunch& p, cudaStream_t stream) {
+cudaError_t launch_one(const MlaLaunch& p, cudaStream_t stream, bool pdl) {
   const MlaSmem S = mla_smem(H, F, p.chunk);
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel<H, F>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, S.total);
   if (e != cudaSuccess) return e;
   dim3 grid(p.num_splits, p.nshards * p.rows);
-  sparse_mla_kernel<H, F><<<grid, kThreads, S.total, stream>>>(p);
-  return cudaGetLastError();
+  return launch_ex(sparse_mla_kernel<H, F>, grid, dim3(kThreads), S.total, stream, pdl, p);
 }
 
 }  // namespace
@@ -613,10 +618,12 @@ int auto_mla_splits(int work_rows, int k, int expected_count) {
   return s;
 }
 
-cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream) {
+cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream, bool pdl) {
   if (p.nshards * p.rows == 0 || p.num_splits == 0) return cudaSuccess;
-  if (p.heads == 16) return p.fp8 ? launch_one<16, true>(p, stream) : launch_one<16, false>(p, stream);
-  if (p.heads == 32) return p.fp8 ? launch_one<32, true>(p, stream) : launch_one<32, false>(p, stream);
+  if (p.heads == 16)
+    return p.fp8 ? launch_one<16, true>(p, stream, pdl) : launch_one<16, false>(p, stream, pdl);
+  if (p.heads == 32)
+    return p.fp8 ? launch_one<32, true>(p, stream, pdl) : launch_one<32, false>(p, stream, pdl);
   return cudaErrorInvalidValue;
 }
 

@@ -184,6 +184,8 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
   const int w = q / P.rows;
   const int r = q - w * P.rows;
   const int k = P.k;
+  pdl_trigger();
+  pdl_wait();  // the scores come from the previous grid
 
   // every CTA of the cluster derives the same n, so all take the same branches
   // and pass the same cluster barriers
@@ -223,7 +225,7 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int i = base + u * kThreads + tid;
-        v[u] = i < nv ? __ldg(src4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = i < nv ? __ldcg(src4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -245,7 +247,7 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
     for (int i = nv * 4 + tid; i < m; i += kThreads) {
-      const float f = __ldg(seg + i);
+      const float f = __ldcg(seg + i);
       nan_seen |= (f != f);
       const uint32_t key = score_key(f);
       kmin = min(kmin, key);
@@ -299,7 +301,7 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
 
   // key of segment position j
   auto key_at = [&](int j) -> uint32_t {
-    return j < cached ? keys[j] : score_key(__ldg(seg + j));
+    return j < cached ? keys[j] : score_key(__ldcg(seg + j));
   };
   // the keys of segment positions j0 .. j0 + 3 below lim (j0 a multiple of 4)
   auto load4 = [&](int j0, int lim, uint32_t* kv, bool* ok) {
@@ -657,7 +659,7 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
       if (self[e]) {
         const int pos = c0 + j0 + e;
         oi[slot] = pos * P.index_stride + off;
-        if (os) os[slot] = all ? __ldg(seg + j0 + e) : key_score(kv[e]);
+        if (os) os[slot] = all ? __ldcg(seg + j0 + e) : key_score(kv[e]);
         ++slot;
       }
     }
@@ -675,25 +677,24 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 template <int C>
-cudaError_t launch_c(const TopkLaunch& p, int rows, cudaStream_t stream) {
+cudaError_t launch_c(const TopkLaunch& p, int rows, cudaStream_t stream, bool pdl) {
   const TopkSmem S = topk_smem(C);
   cudaError_t e =
       cudaFuncSetAttribute(topk_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, S.total);
   if (e != cudaSuccess) return e;
-  topk_kernel<C><<<rows * C, kThreads, S.total, stream>>>(p, S);
-  return cudaGetLastError();
+  return launch_ex(topk_kernel<C>, dim3(rows * C), dim3(kThreads), S.total, stream, pdl, p, S);
 }
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkLaunch& p, cudaStream_t stream) {
+cudaError_t launch_topk(const TopkLaunch& p, cudaStream_t stream, bool pdl) {
   const int rows = p.nshards * p.rows;
   if (rows == 0) return cudaSuccess;
   // the widest cluster that still runs every row at once (one CTA per SM)
   const int sms = num_sms() > 0 ? num_sms() : 148;
-  if (rows * 4 <= sms) return launch_c<4>(p, rows, stream);
-  if (rows * 2 <= sms) return launch_c<2>(p, rows, stream);
-  return launch_c<1>(p, rows, stream);
+  if (rows * 4 <= sms) return launch_c<4>(p, rows, stream, pdl);
+  if (rows * 2 <= sms) return launch_c<2>(p, rows, stream, pdl);
+  return launch_c<1>(p, rows, stream, pdl);
 }
 
 }  // namespace dsa
