@@ -33,15 +33,13 @@ constexpr int kCompute = 256;                 // warps 0..7: tensor-core math
 constexpr int kGather = 64;                   // warps 8..9: the row gather
 constexpr int kThreads = kCompute + kGather;
 constexpr int kTile = 64;                 // tokens per tile
-constexpr int kMaxK = 4096;               // largest selection the entry points accept
-constexpr int kMaxPerThread = (kMaxK + kThreads - 1) / kThreads;
 constexpr int kRowB = kKvDim * 2 + 16;    // padded smem row of 576 16-bit values
 constexpr int kPRowB = kTile * 2 + 16;    // padded smem row of P
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct MlaSmem {
-  int off_q, off_kv, off_raw, off_p, off_red, off_rowoff, off_kscale, off_misc, off_bar, total;
+  int off_q, off_kv, off_raw, off_p, off_red, off_kscale, off_misc, off_bar, total;
   int kv_bufs;
 };
 
@@ -59,8 +57,6 @@ __host__ __device__ inline MlaSmem mla_smem(int heads, int fp8, int chunk) {
   off += (fp8 ? 1 : 2) * heads * kPRowB;  // bf16 path: P = hi + lo
   s.off_red = off;
   off += 2 * 8 * heads * 4;
-  s.off_rowoff = off;
-  off += chunk * 8;
   s.off_kscale = off;
   off += fp8 ? chunk * 4 : 0;
   s.off_misc = off;
@@ -131,7 +127,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
   uint8_t* raw_s = smem + S.off_raw;
   uint8_t* p_s = smem + S.off_p;
   float* red = reinterpret_cast<float*>(smem + S.off_red);      // [2][TGS][H]
-  long long* rowoff = reinterpret_cast<long long*>(smem + S.off_rowoff);
   float* kscale_s = reinterpret_cast<float*>(smem + S.off_kscale);
   int* misc = reinterpret_cast<int*>(smem + S.off_misc);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S.off_bar);  // full[2], empty[2]
@@ -152,8 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
   // this grid is its programmatic dependent) does not write: they are fetched
   // while it finishes.  The bf16 query copy stays in flight meanwhile.
   const uint16_t* qsrc = P.q + static_cast<long long>(r) * H * kKvDim;
-  if (!kFp8) {
-    for (int c = tid; c < H * 72; c += kThreads) {
+  if (!kFp8 && tid < kCompute) {
+    for (int c = tid; c < H * 72; c += kCompute) {
       const int h = c / 72, cc = c - h * 72;
       cp_async16(smem_u32(q_s + h * kRowB + cc * 16), qsrc + h * kKvDim + cc * 8);
     }
@@ -175,6 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
     *abort_flag = 0;
     fence_mbar_init();
   }
+  __syncthreads();  // the request index and the barriers
+  const int b = misc[0];
   pdl_wait();  // the selections come from the previous grid
 
   int cnt = __ldcg(P.count + qrow);
@@ -193,90 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
     for (int h = tid; h < H; h += kThreads) out_l[h] = -__int_as_float(0x7f800000);
     if (direct)
       for (int i = tid; i < H * kVDim; i += kThreads) out_o[i] = 0.0f;
-    if (!kFp8) cp_async_wait<0>();  // no copy may land after the CTA leaves
+    if (!kFp8 && tid < kCompute) cp_async_wait<0>();  // no copy may land after the CTA leaves
     return;
   }
 
-  // the split's selected positions: all loads issued before any is used
-  const int32_t* ilist = P.idx + static_cast<long long>(qrow) * P.k + begin;
-  int tv[kMaxPerThread];
-#pragma unroll
-  for (int j = 0; j < kMaxPerThread; ++j) {
-    const int i = tid + j * kThreads;
-    tv[j] = i < ntok ? __ldcg(ilist + i) : 0;
-  }
-
-  // bf16: wait for the query copy; fp8: the query as f16 with a per-head
-  // power of two
-  if (!kFp8) {
-    cp_async_wait<0>();
-    if (tid < H) qexp[tid] = P.sm_scale * kLog2e;
-  } else {
-    // one warp per head: max |q| -> exponent -> scaled f16 copy
-    for (int h = warp; h < H; h += kThreads / 32) {
-      const uint16_t* src = qsrc + h * kKvDim;
-      uint32_t mx = 0;
-      for (int i = lane; i < kKvDim; i += 32) mx = max(mx, static_cast<uint32_t>(src[i] & 0x7FFFu));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const int ebits = static_cast<int>(mx >> 7);
-      const int e = (ebits == 0) ? 0 : max(-100, min(100, 141 - ebits));
-      const float sc = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
-      for (int i = lane; i < kKvDim / 2; i += 32) {
-        const uint32_t two = *reinterpret_cast<const uint32_t*>(src + 2 * i);
-        const float lo = __uint_as_float(two << 16) * sc;
-        const float hi = __uint_as_float(two & 0xFFFF0000u) * sc;
-        *reinterpret_cast<uint32_t*>(q_s + h * kRowB + i * 4) = pack2<true>(lo, hi);
-      }
-      if (lane == 0)
-        qexp[h] = P.sm_scale * kLog2e * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-    }
-  }
-  __syncthreads();
-  const int b = misc[0];
   if (tid == 0 && b < 0) raise_err(P.d_err, DSA_DEVERR_ROWS);
-
-  // resolve the positions to element offsets: block-table loads in one batch,
-  // then (fp8) the token scales in one batch
-  const int32_t* bt = P.block_table[w];
-  const int psz = P.page_size;
-  const long long span = static_cast<long long>(P.max_blocks[w]) * psz;
-  long long offv[kMaxPerThread];
-#pragma unroll
-  for (int j = 0; j < kMaxPerThread; ++j) {
-    const int i = tid + j * kThreads;
-    offv[j] = -1;
-    if (i < ntok) {
-      const int t = tv[j];
-      if (b >= 0 && t >= 0 && static_cast<long long>(t) < span) {
-        const int lp = t / psz;
-        const int pg = bt ? __ldg(bt + static_cast<long long>(b) * P.max_blocks[w] + lp)
-                          : b * P.max_blocks[w] + lp;
-        offv[j] = static_cast<long long>(pg) * psz + (t - lp * psz);
-        tv[j] = pg;
-      } else {
-        raise_err(P.d_err, DSA_DEVERR_INDEX);
-      }
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < kMaxPerThread; ++j) {
-    const int i = tid + j * kThreads;
-    if (i < ntok && offv[j] >= 0 && (tv[j] < 0 || tv[j] >= P.num_pages[w])) {
-      raise_err(P.d_err, DSA_DEVERR_PAGE);
-      offv[j] = -1;
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < kMaxPerThread; ++j) {
-    const int i = tid + j * kThreads;
-    if (i < ntok) {
-      rowoff[i] = offv[j];
-      if (kFp8) kscale_s[i] = offv[j] >= 0 ? __ldg(P.kscale[w] + offv[j]) : 0.0f;
-    }
-  }
-  __syncthreads();
-
   const uint8_t* kvbase = static_cast<const uint8_t*>(P.kv[w]);
   const int ntiles = (ntok + kTile - 1) / kTile;
 
@@ -287,8 +205,38 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
     // (the copy engine takes whole rows; scattered 16-byte copies were bound
     // by their issue rate) and arrives on the tile's barrier with the bytes it
     // expects; a row past the split is zero-filled before the arrival.
+    // Every thread resolves its own row of the next tile (selection ->
+    // block table -> element offset, and the fp8 token scale) right after it
+    // issues the current tile's copy, while the compute warps work.
     const int gt = tid - kCompute;  // the tile row this thread moves
     constexpr uint32_t kRowBytes = kFp8 ? kKvDim : kKvDim * 2;
+    const int32_t* ilist = P.idx + static_cast<long long>(qrow) * P.k + begin;
+    const int32_t* bt = P.block_table[w];
+    const int psz = P.page_size;
+    const long long span = static_cast<long long>(P.max_blocks[w]) * psz;
+    auto resolve = [&](int tile, long long& off, float& ks) {
+      off = -1;
+      ks = 0.0f;
+      const int i = tile * kTile + gt;
+      if (tile >= ntiles || i >= ntok) return;  // no row: zero-filled
+      const int t = __ldcg(ilist + i);
+      if (b < 0 || t < 0 || static_cast<long long>(t) >= span) {
+        raise_err(P.d_err, DSA_DEVERR_INDEX);
+        return;
+      }
+      const int lp = t / psz;
+      const int pg = bt ? __ldg(bt + static_cast<long long>(b) * P.max_blocks[w] + lp)
+                        : b * P.max_blocks[w] + lp;
+      if (pg < 0 || pg >= P.num_pages[w]) {
+        raise_err(P.d_err, DSA_DEVERR_PAGE);
+        return;
+      }
+      off = static_cast<long long>(pg) * psz + (t - lp * psz);
+      if (kFp8) ks = __ldg(P.kscale[w] + off);
+    };
+    long long off_next;
+    float ks_next;
+    resolve(0, off_next, ks_next);
     int issued = 0;
     for (int tile = 0; tile < ntiles; ++tile) {
       const int buf = tile & 1, use = tile >> 1;
@@ -297,9 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
         break;
       const int t0 = tile * kTile;
       const uint32_t full = smem_u32(bars + buf);
+      const long long off = off_next;
+      if (kFp8 && t0 + gt < ntok) kscale_s[t0 + gt] = ks_next;  // read after the tile's barrier
       uint8_t* dst = kFp8 ? raw_s + buf * kTile * kKvDim + gt * kKvDim
                           : kv_s + buf * kTile * kRowB + gt * kRowB;
-      const long long off = (t0 + gt < ntok) ? rowoff[t0 + gt] : -1;
       if (off >= 0) {
         mbar_arrive_expect_tx(full, kRowBytes);
         bulk_copy_g2s(smem_u32(dst), kvbase + off * kRowBytes, kRowBytes, full);
@@ -309,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
         mbar_arrive(full);
       }
       ++issued;
+      resolve(tile + 1, off_next, ks_next);
     }
     // after an abort the compute warps stop waiting: every copy still in
     // flight must land before the CTA exits
@@ -319,6 +269,44 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
     }
   } else {
     // ================================================= compute (warps 0..7)
+    // bf16: wait for the query copy.  fp8: the query as f16 with a per-head
+    // power of two; every warp loads all of its heads before converting any
+    if (!kFp8) {
+      cp_async_wait<0>();
+      if (tid < H) qexp[tid] = P.sm_scale * kLog2e;
+    } else {
+      constexpr int kHpw = H / (kCompute / 32);  // heads per warp
+      uint32_t qv[kHpw][kKvDim / 64];
+#pragma unroll
+      for (int x = 0; x < kHpw; ++x) {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(qsrc + (warp + x * 8) * kKvDim);
+#pragma unroll
+        for (int j = 0; j < kKvDim / 64; ++j) qv[x][j] = __ldg(src + lane + 32 * j);
+      }
+#pragma unroll
+      for (int x = 0; x < kHpw; ++x) {
+        const int h = warp + x * 8;
+        uint32_t mx = 0;
+#pragma unroll
+        for (int j = 0; j < kKvDim / 64; ++j)
+          mx = max(mx, max(qv[x][j] & 0x7FFFu, (qv[x][j] >> 16) & 0x7FFFu));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const int ebits = static_cast<int>(mx >> 7);
+        const int e = (ebits == 0) ? 0 : max(-100, min(100, 141 - ebits));
+        const float sc = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+#pragma unroll
+        for (int j = 0; j < kKvDim / 64; ++j) {
+          const uint32_t two = qv[x][j];
+          const float lo = __uint_as_float(two << 16) * sc;
+          const float hi = __uint_as_float(two & 0xFFFF0000u) * sc;
+          *reinterpret_cast<uint32_t*>(q_s + h * kRowB + (lane + 32 * j) * 4) = pack2<true>(lo, hi);
+        }
+        if (lane == 0)
+          qexp[h] = P.sm_scale * kLog2e * __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      }
+    }
+    named_bar_sync(1, kCompute);  // the query is in shared memory
     // per-thread state: O accumulators for dims [64*warp, 64*warp+64) of all heads
     float o[MT][8][4];
 #pragma unroll
