@@ -38,8 +38,9 @@ constexpr int kTileT = 128;
 constexpr int kThreads = 256;
 constexpr int kOpBytes = kTileT * kIdxDim * 2;     // 32 KB bf16 key tile
 constexpr int kRawFp8Bytes = kTileT * kIdxDim;     // 16 KB e4m3 key tile
-// an fp8 stage: the e4m3 tile, its 128 fp32 token scales, padding to the
-// 1024-byte alignment of the 128B-swizzled operand
+// an fp8 stage: the e4m3 tile, then the (page, slot) of its two 64-token
+// chunks for the epilogue's scale loads, padded to the 1024-byte alignment
+// of the 128B-swizzled operand
 constexpr int kFp8StageBytes = kRawFp8Bytes + 1024;
 constexpr int kHalfBf16Box = 64 * 64 * 2;          // one TMA box: 64 tokens x 64 dims
 constexpr int kSmemLimit = 227 * 1024;
@@ -305,21 +306,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pages[h] = pg;
             slots[h] = t0 % P.page_size;
-            bytes += kFp8 ? 64u * 128u + 64u * 4u : 2u * kHalfBf16Box;
+            bytes += kFp8 ? 64u * 128u : 2u * kHalfBf16Box;
           }
           const uint32_t fb = bar(B_KFULL + stage);
-          mbar_arrive_expect_tx(fb, bytes);
           const uint32_t dst = ring + stage * L.stage_bytes;
+          if (kFp8) {
+            // where the epilogue finds the tile's token scales (it loads its
+            // token's scale itself); released to it by the arrival below
+            int* where = reinterpret_cast<int*>(sbase + L.off_ring + stage * L.stage_bytes +
+                                                kRawFp8Bytes);
+            where[0] = pages[0];
+            where[1] = pages[1];
+            where[2] = slots[0];
+            where[3] = slots[1];
+          }
+          mbar_arrive_expect_tx(fb, bytes);
           for (int h = 0; h < 2; ++h) {
             if (pages[h] < 0) continue;
             if (kFp8) {
               tma_load_3d(dst + h * 8192, &P.kmap[sl], fb, 0, slots[h], pages[h]);
-              // the chunk's 64 token scales (256 B, 16-byte aligned: the scale
-              // array is, and a chunk starts at a multiple of 64 tokens)
-              bulk_copy_g2s(dst + kRawFp8Bytes + h * 256,
-                            P.kscale[sl] + static_cast<long long>(pages[h]) * P.page_size +
-                                slots[h],
-                            256u, fb);
             } else {
               tma_load_3d(dst + h * 8192, &P.kmap[sl], fb, 0, slots[h], pages[h]);
               tma_load_3d(dst + 16384 + h * 8192, &P.kmap[sl], fb, 64, slots[h], pages[h]);
@@ -545,12 +550,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = wk.tile * kTileT + et;
         float kscale = 1.0f;
         if (kFp8) {
-          // the tile's token scales sit behind its keys in the stage, which
-          // stays filled until this warp's release below
+          // the token's scale, from the (page, slot) the producer left behind
+          // the keys; loaded now, used after the accumulator wait
           const bool got = mbar_wait(bar(B_KFULL + stage), phase, abort_flag);
           if (!__all_sync(0xffffffffu, got)) break;
-          kscale = reinterpret_cast<const float*>(sbase + L.off_ring + stage * L.stage_bytes +
-                                                  kRawFp8Bytes)[et];
+          const int* where = reinterpret_cast<const int*>(sbase + L.off_ring +
+                                                          stage * L.stage_bytes + kRawFp8Bytes);
+          const int h = et >> 6;
+          const int pg = where[h];
+          kscale = pg >= 0 ? __ldg(P.kscale[sl] + static_cast<long long>(pg) * P.page_size +
+                                   where[2 + h] + (et & 63))
+                           : 0.0f;
         }
         float* out_base = P.scores + static_cast<long long>(sl) * P.shard_stride;
         const int nr = wk.pi.nr;
