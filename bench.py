@@ -56,7 +56,7 @@ def parse():
                     help="time the fused step on configuration 0..4 instead (device time only, "
                          "one JSON line; the contract line is the default configuration 1)")
     ap.add_argument("--batch", type=int, default=None, help="requests of configuration 4")
-    ap.add_argument("--kernel", default=None, choices=["indexer", "topk", "mla"],
+    ap.add_argument("--kernel", default=None, choices=["indexer", "topk", "mla", "cache_write"],
                     help="time one kernel of the step alone on the same workload (a short "
                          "run for profilers: W warm-up launches, then K timed ones)")
     return ap.parse_args()
@@ -304,6 +304,8 @@ def run_kernel_only(args):
     valid = (dw.rows.row_pos + 1).to(torch.int32)
     mla_ws = torch.empty(max(1, api.dsa_sparse_mla_decode_workspace_size(R, H, k, lay.num_splits)),
                          dtype=torch.uint8, device=dev)
+    if args.kernel == "cache_write":
+        return time_cache_write(args, dw, spec, dev, err)
     fn = {
         "indexer": lambda: api.dsa_indexer_scores(dw.q_idx, dw.w_idx, dw.idx_k, dw.rows, scores,
                                                   err),
@@ -330,6 +332,50 @@ def run_kernel_only(args):
         raise SystemExit("device error word set")
     print(json.dumps({"kernel": args.kernel, "workload": spec.name, "launches": args.steps,
                       "us_mean": round(1e3 * float(np.mean(ms)), 2)}), flush=True)
+
+
+def time_cache_write(args, dw, spec, dev, err):
+    """The cache write of one decode step (one new token per request, at the
+    row's position) and of a 1024-token append per request, into the
+    workload's own caches (their contents change: this mode times only)."""
+    import torch
+
+    from dsa_sparse_attention_decode_gb300 import api
+
+    B = dw.rows.num_reqs
+    flush_w = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+    g = torch.Generator(device=dev).manual_seed(11)
+    res = {}
+    for name, per_req in (("decode_step", 1), ("append_1024", 1024)):
+        N = B * per_req
+        req = torch.arange(B, dtype=torch.int32, device=dev).repeat_interleave(per_req)
+        last = dw.rows.row_pos[dw.rows.row_start[1:].long() - 1]
+        pos = (last.repeat_interleave(per_req) -
+               torch.arange(per_req, dtype=torch.int32, device=dev).repeat(B)).to(torch.int32)
+        kv_in = torch.randn((N, 576), generator=g, device=dev).to(torch.bfloat16).view(torch.int16)
+        ix_in = torch.randn((N, 128), generator=g, device=dev).to(torch.bfloat16).view(torch.int16)
+        ms = []
+        for i in range(args.warmup + args.steps):
+            flush_w.zero_()
+            flush_r.sum()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            api.dsa_cache_write(kv_in, req, pos, B, [dw.kv], err, idx_in=ix_in, idx_k=[dw.idx_k])
+            b.record()
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                ms.append(a.elapsed_time(b))
+        us = 1e3 * float(np.median(ms))
+        esz = 2 if spec.dtype == "bf16" else 1
+        byts = N * (576 * 2 + 128 * 2 + 576 * esz + 128 * esz + (8 if esz == 1 else 0) + 8)
+        res[name] = {"tokens": N, "us": round(us, 2), "tokens_per_s": round(N / (us * 1e-6), 1),
+                     "algorithmic_bytes": byts, "gbs": round(byts / (us * 1e-6) / 1e9, 1)}
+    if api.dsa_read_error(err) != 0:
+        raise SystemExit("device error word set")
+    print(json.dumps({"kernel": "cache_write", "workload": spec.name, "launches": args.steps,
+                      **res}), flush=True)
 
 
 def run_product(args):

@@ -119,6 +119,9 @@ PROTOTYPES = {
                                               c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dsa_lse_merge": (c_int, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p,
                               c_void_p, c_void_p]),
+    "dsa_cache_write": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float,
+                                POINTER(DsaPagedCache), POINTER(DsaPagedCache), c_int32, c_void_p,
+                                c_void_p]),
     "dsa_decode_workspace_size": (c_size_t, [POINTER(DsaDecodeDesc)]),
     "dsa_decode_workspace_layout": (c_int, [POINTER(DsaDecodeDesc), POINTER(DsaDecodeLayout)]),
     "dsa_decode": (c_int, [POINTER(DsaDecodeDesc), c_void_p, c_size_t, c_void_p, c_void_p]),

@@ -113,6 +113,20 @@ def dsa_topk(scores, valid_len, k: int, out_idx, out_count, d_err, out_score=Non
            "dsa_topk")
 
 
+def dsa_cache_write(kv_in, tok_req, tok_pos, num_reqs: int, kv: Sequence[PagedCache], d_err,
+                    idx_in=None, idx_k: Optional[Sequence[PagedCache]] = None,
+                    rope_base: float = 10000.0, stream=None):
+    """One decode step's cache write: the new tokens' latent rows (kv_in
+    [N, 576] bf16 bits) and index-K rows (idx_in [N, 128]), RoPE on their last
+    64 dims, stored on the owner shard (pos % W) of `kv` / `idx_k`."""
+    W = len(kv)
+    kvc = (C.DsaPagedCache * W)(*[c.c() for c in kv])
+    ixc = (C.DsaPagedCache * W)(*[c.c() for c in idx_k]) if idx_k is not None else None
+    _check(C.lib().dsa_cache_write(_ptr(kv_in), _ptr(idx_in), _ptr(tok_req), _ptr(tok_pos),
+                                   int(tok_pos.shape[0]), int(num_reqs), float(rope_base), kvc,
+                                   ixc, W, _ptr(d_err), _stream(stream)), "dsa_cache_write")
+
+
 def dsa_shard_topk_merge(cand_score, cand_pos, cand_count, out_idx, out_count, owned_local,
                          owned_count, d_err, stream=None):
     W, R, k = (int(x) for x in cand_score.shape)

@@ -3,6 +3,7 @@
 // on the host and only enqueues kernels on the caller's stream.
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
@@ -338,6 +339,55 @@ static int check_decode(const dsa_decode_desc* d) {
     if (!aligned16(d->q_idx) || !aligned16(d->q) || !aligned16(d->out)) return DSA_ERR_INVALID_ARG;
   }
   return DSA_OK;
+}
+
+int dsa_cache_write(const uint16_t* kv_in, const uint16_t* idx_in, const int32_t* tok_req,
+                    const int32_t* tok_pos, int32_t num_tokens, int32_t num_reqs,
+                    float rope_base, const dsa_paged_cache* kv, const dsa_paged_cache* idx_k,
+                    int32_t num_shards, int32_t* d_err, void* stream) {
+  if (num_tokens < 0 || num_reqs < 1 || num_shards < 1 || num_shards > kMaxShards ||
+      !(rope_base > 0.0f) || d_err == nullptr || kv == nullptr)
+    return DSA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return DSA_OK;
+  if (kv_in == nullptr || tok_req == nullptr || tok_pos == nullptr || !aligned16(kv_in))
+    return DSA_ERR_INVALID_ARG;
+  if (idx_in != nullptr && (idx_k == nullptr || !aligned16(idx_in))) return DSA_ERR_INVALID_ARG;
+  CacheWriteLaunch L{};
+  const int page = kv[0].page_size;
+  for (int w = 0; w < num_shards; ++w) {
+    int st = check_cache(&kv[w], kKvDim);
+    if (st != DSA_OK) return st;
+    if (kv[w].dtype != kv[0].dtype || kv[w].page_size != page) return DSA_ERR_INVALID_ARG;
+    L.kv.data[w] = const_cast<void*>(kv[w].data);
+    L.kv.scale[w] = const_cast<float*>(kv[w].scale);
+    L.kv.block_table[w] = kv[w].block_table;
+    L.kv.num_pages[w] = kv[w].num_pages;
+    L.kv.max_blocks[w] = kv[w].max_blocks;
+    if (idx_in != nullptr) {
+      st = check_cache(&idx_k[w], kIdxDim);
+      if (st != DSA_OK) return st;
+      if (idx_k[w].dtype != idx_k[0].dtype || idx_k[w].page_size != page)
+        return DSA_ERR_INVALID_ARG;
+      L.idx.data[w] = const_cast<void*>(idx_k[w].data);
+      L.idx.scale[w] = const_cast<float*>(idx_k[w].scale);
+      L.idx.block_table[w] = idx_k[w].block_table;
+      L.idx.num_pages[w] = idx_k[w].num_pages;
+      L.idx.max_blocks[w] = idx_k[w].max_blocks;
+    }
+  }
+  L.kv.fp8 = kv[0].dtype == DSA_DTYPE_FP8_E4M3;
+  L.idx.fp8 = idx_in != nullptr && idx_k[0].dtype == DSA_DTYPE_FP8_E4M3;
+  L.kv_in = kv_in;
+  L.idx_in = idx_in;
+  L.tok_req = tok_req;
+  L.tok_pos = tok_pos;
+  L.num_tokens = num_tokens;
+  L.num_reqs = num_reqs;
+  L.W = num_shards;
+  L.page_size = page;
+  for (int i = 0; i < 32; ++i) L.theta[i] = std::pow(static_cast<double>(rope_base), -i / 32.0);
+  L.d_err = d_err;
+  return cuda_status(launch_cache_write(L, static_cast<cudaStream_t>(stream)));
 }
 
 int dsa_decode_workspace_layout(const dsa_decode_desc* d, dsa_decode_layout* lay) {

@@ -116,6 +116,28 @@ struct MlaLaunch {
 cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream, bool pdl = false);
 int auto_mla_splits(int work_rows, int k, int expected_count);
 
+// ------------------------------------------------------------- cache write
+
+struct CacheWriteSide {    // the shard caches of one kind (latent or index-K)
+  void* data[DSA_MAX_SHARDS];
+  float* scale[DSA_MAX_SHARDS];
+  const int32_t* block_table[DSA_MAX_SHARDS];
+  int32_t num_pages[DSA_MAX_SHARDS];
+  int32_t max_blocks[DSA_MAX_SHARDS];
+  int32_t fp8;
+};
+struct CacheWriteLaunch {
+  CacheWriteSide kv, idx;
+  const uint16_t* kv_in;   // [N][576] bf16
+  const uint16_t* idx_in;  // [N][128] bf16 or NULL
+  const int32_t* tok_req;
+  const int32_t* tok_pos;
+  int32_t num_tokens, num_reqs, W, page_size;
+  double theta[32];        // rope_base^(-i/32), i < 32: the rotation rates
+  int32_t* d_err;
+};
+cudaError_t launch_cache_write(const CacheWriteLaunch& p, cudaStream_t stream);
+
 // ------------------------------------------------------------- LSE merge
 
 cudaError_t launch_lse_merge(const float* O_parts, const float* lse_parts, int parts,

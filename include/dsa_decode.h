@@ -348,6 +348,50 @@ typedef struct {
   int32_t* out_topk_count;
 } dsa_decode_desc;
 
+/*
+ * dsa_cache_write -- one decode step's cache write: every new token's latent
+ * KV row and index-K row, RoPE applied, stored (quantized for fp8 caches) in
+ * the cache of the shard that owns the token.  DCP page, Modifications /
+ * Writes (MLA KV and indexer K land only on the owner rank, slot % W ==
+ * rank; the fused RoPE + KV-cache write) and the decode-gap analysis (the
+ * owner-rule write location computed once per step inside the write kernel
+ * instead of by many small kernels).
+ *
+ * Token j < num_tokens belongs to request tok_req[j] (< num_reqs) at logical
+ * position tok_pos[j] (>= 0):
+ *   kv_in:   device bf16 [num_tokens][576], the latent row; its last 64 dims
+ *            are given before RoPE
+ *   idx_in:  device bf16 [num_tokens][128], the index-K row; its last 64
+ *            dims are given before RoPE (NULL: no index-K write)
+ *   RoPE:    on the last 64 dims of each row, pairs (2i, 2i+1), i < 32:
+ *            a = pos * rope_base^(-i/32) (the angle is formed in double),
+ *            (x, y) -> (x cos a - y sin a, x sin a + y cos a)
+ *   kv, idx_k: [num_shards] caches (row_elems 576 and 128, one dtype per
+ *            array, the same page size); token j goes to shard w = pos % W
+ *            at local position p = pos / W: page
+ *            block_table_w[req * max_blocks_w + p / page_size] (req *
+ *            max_blocks_w + p / page_size when block_table is NULL), slot
+ *            p % page_size.  The caches' data and scale arrays are written.
+ *   bf16 caches store the RNE bf16 of every value.  fp8 caches store the
+ *   e4m3 codes (round to nearest even, saturating at +-448) of value / s,
+ *   s = max|value| / 448 over the row (fp32; s = 1 for an all-zero row), and
+ *   s in the token's scale slot.
+ *
+ * Only each token's owner slot is written; nothing else is touched.  Two
+ * tokens with the same (request, position) write the same slot in no
+ * defined order.
+ * Errors: DSA_ERR_INVALID_ARG for NULL pointers, bad sizes, num_shards
+ * outside 1..DSA_MAX_SHARDS, caches of the wrong width or of mixed dtype or
+ * page size.  Device: DSA_DEVERR_ROWS (request out of range), DSA_DEVERR_POS
+ * (negative position or one past the block table), DSA_DEVERR_PAGE (page id
+ * out of range); such a token is not written.
+ */
+int dsa_cache_write(const uint16_t* kv_in, const uint16_t* idx_in, const int32_t* tok_req,
+                    const int32_t* tok_pos, int32_t num_tokens, int32_t num_reqs,
+                    float rope_base, const dsa_paged_cache* kv,
+                    const dsa_paged_cache* idx_k, int32_t num_shards, int32_t* d_err,
+                    void* stream);
+
 /* Where dsa_decode keeps its intermediates inside the workspace (byte
  * offsets; -1 = not used).  scores is [W][num_rows][ld_scores] fp32. */
 typedef struct {

@@ -30,7 +30,12 @@ design notes):
   at the k-th place goes to the lower position); the selected positions are
   listed in ascending order; with fewer valid tokens than k all are kept;
 * a row at position ``pos`` sees tokens 0..pos;
-* an empty partial (no tokens) has LSE = -inf and contributes nothing.
+* an empty partial (no tokens) has LSE = -inf and contributes nothing;
+* cache write (Modifications / Writes and the fused RoPE + cache write the
+  page names): RoPE on the last 64 dims of each row in consecutive pairs,
+  pair i rotated counter-clockwise by pos * base^(-i/32); a token is stored
+  only on shard pos % W at local position pos // W; fp8 rows store e4m3 codes
+  of value / s with s = max|value| / 448, both decided in fp32.
 
 Parity status: every function here is pinned by the CPU tests in
 ``tests/test_oracle_pins.py`` (closed forms, brute force, library routines,
@@ -279,3 +284,93 @@ def decode_row_sharded(wl, r: int, W: Optional[int] = None):
         ls.append(l_w)
     O, lse = lse_merge(np.stack(Os), np.stack(ls))
     return dict(idx=sel, owned=owned, O=O, lse=lse, cand_scores=cs, cand_pos=cp)
+
+
+# ----------------------------------------------------------------------------
+# cache write (the step that appends new tokens to the caches)
+# ----------------------------------------------------------------------------
+#
+# DCP page, Modifications / Writes: MLA KV and indexer K land only on the
+# owner rank (slot % W); the page names a fused RoPE + KV-cache write.  The
+# page gives no RoPE convention; the reading used here (and in the library):
+# the last 64 dims of each row are the rope dims, taken in consecutive pairs
+# (2i, 2i + 1), i < 32, rotated counter-clockwise by pos * base^(-i/32).
+# fp8 rows: scale s = max|value| / 448 (1 for an all-zero row) and codes
+# e4m3(value / s), both taken in fp32 (the kernel's precision), round to
+# nearest even, saturating at +-448.
+
+_E4M3_POS = None
+
+
+def _e4m3_positive_values() -> np.ndarray:
+    """Values of the 127 finite non-negative e4m3 codes 0x00..0x7E, in code
+    order (which is value order)."""
+    global _E4M3_POS
+    if _E4M3_POS is None:
+        _E4M3_POS = e4m3_code_to_f64(np.arange(127, dtype=np.uint8))
+    return _E4M3_POS
+
+
+def e4m3_encode_rne(x: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 code of every value (ties to the even code, i.e. the even
+    mantissa), magnitudes above 448 saturating to 448.  The sign goes to bit 7
+    (a negative value that rounds to zero keeps its sign)."""
+    x = np.asarray(x, dtype=np.float64)
+    vals = _e4m3_positive_values()
+    m = np.minimum(np.abs(x), vals[-1])
+    hi = np.searchsorted(vals, m, side="left")        # first value >= m
+    hi = np.minimum(hi, len(vals) - 1)
+    lo = np.maximum(hi - 1, 0)
+    dl = m - vals[lo]
+    dh = vals[hi] - m
+    pick_hi = (dh < dl) | ((dh == dl) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(vals[hi] == m, hi, code)           # exact hits
+    return (code | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+
+
+def bf16_round_rne(x: np.ndarray) -> np.ndarray:
+    """Nearest bf16 (bits) of float64 values, ties to even: the two bf16
+    neighbours of x come from truncating its float32 pattern."""
+    x = np.asarray(x, dtype=np.float64)
+    f = x.astype(np.float32)
+    u = f.view(np.uint32) & np.uint32(0xFFFF0000)
+    lo = u.view(np.float32).astype(np.float64)
+    up = (u + np.uint32(0x10000)).view(np.float32).astype(np.float64)
+    # lo is the neighbour towards zero, up the one away from it
+    dlo = np.abs(x - lo)
+    dup = np.abs(up - x)
+    even_lo = ((u >> np.uint32(16)) & np.uint32(1)) == 0
+    take_up = (dup < dlo) | ((dup == dlo) & ~even_lo)
+    bits = np.where(take_up, (u + np.uint32(0x10000)), u) >> np.uint32(16)
+    return bits.astype(np.uint16)
+
+
+def rope_last64(row: np.ndarray, pos: int, base: float) -> np.ndarray:
+    """The row with its last 64 dims rotated pairwise: pair i = (x, y) at
+    dims (D-64+2i, D-64+2i+1) becomes (x cos a - y sin a, x sin a + y cos a),
+    a = pos * base^(-i/32)."""
+    out = np.array(row, dtype=np.float64, copy=True)
+    D = out.shape[-1]
+    i = np.arange(32)
+    a = float(pos) * np.power(float(base), -i / 32.0)
+    x = out[..., D - 64::2].copy()
+    y = out[..., D - 63::2].copy()
+    out[..., D - 64::2] = x * np.cos(a) - y * np.sin(a)
+    out[..., D - 63::2] = x * np.sin(a) + y * np.cos(a)
+    return out
+
+
+def cache_write_row(row_bits: np.ndarray, pos: int, base: float, dtype: str):
+    """What the cache write stores for one token's row: (stored bf16 bits or
+    e4m3 codes, fp32 scale or None, the exact post-RoPE values in float64)."""
+    exact = rope_last64(bf16_bits_to_f64(row_bits), pos, base)
+    if dtype == "bf16":
+        return bf16_round_rne(exact), None, exact
+    if dtype == "fp8_e4m3":
+        x32 = exact.astype(np.float32)
+        amax = np.float32(np.abs(x32).max())
+        s = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+        q = (x32 / s).astype(np.float32)
+        return e4m3_encode_rne(q), s, exact
+    raise ValueError(dtype)

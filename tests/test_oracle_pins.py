@@ -277,3 +277,93 @@ def test_candidate_merge_equals_global_topk(W):
     assert np.array_equal(sel, want)
     for w in range(W):
         assert np.array_equal(owned[w], want[want % W == w] // W)
+
+
+# ----------------------------------------------------------------------------
+# cache write: e4m3 / bf16 rounding, RoPE, the stored row
+# ----------------------------------------------------------------------------
+
+
+def test_e4m3_encoder_roundtrip_ties_and_saturation():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = orc.e4m3_code_to_f64(codes)
+    fin = ~np.isnan(vals)
+    assert np.array_equal(orc.e4m3_encode_rne(vals[fin]), codes[fin])
+    pos = orc.e4m3_code_to_f64(np.arange(127, dtype=np.uint8))
+    mids = (pos[:-1] + pos[1:]) / 2
+    got = orc.e4m3_encode_rne(mids).astype(np.int64)
+    lo = np.arange(126)
+    assert np.array_equal(got, np.where(lo % 2 == 0, lo, lo + 1)), "ties go to the even code"
+    assert np.array_equal(orc.e4m3_encode_rne(-mids).astype(np.int64), got | 0x80)
+    assert list(orc.e4m3_encode_rne(np.array([448.0, 449.0, 1e30, -1e30]))) == [0x7E, 0x7E, 0x7E, 0xFE]
+    assert orc.e4m3_encode_rne(np.array([2.0 ** -10]))[0] == 0   # half the smallest step: even (0)
+    assert orc.e4m3_encode_rne(np.array([2.0 ** -10 * 1.01]))[0] == 1
+
+
+def test_e4m3_encoder_against_torch():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8 in this torch")
+    rng = np.random.default_rng(5)
+    x = np.concatenate([rng.standard_normal(20000) * 60, rng.standard_normal(5000) * 1e-2])
+    x = np.clip(x, -448, 448).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(orc.e4m3_encode_rne(x.astype(np.float64)), ref)
+
+
+def test_bf16_rounding_against_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(6)
+    x = (rng.standard_normal(50000) * np.exp(rng.uniform(-20, 20, 50000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(orc.bf16_round_rne(x.astype(np.float64)), ref)
+
+
+def test_rope_closed_forms():
+    base = 10000.0
+    rng = np.random.default_rng(7)
+    row = rng.standard_normal(576)
+    assert np.array_equal(orc.rope_last64(row, 0, base), row)          # position 0: identity
+    out = orc.rope_last64(row, 12345, base)
+    assert np.array_equal(out[:512], row[:512])                         # nope dims untouched
+    n0 = row[512::2] ** 2 + row[513::2] ** 2
+    n1 = out[512::2] ** 2 + out[513::2] ** 2
+    assert np.allclose(n0, n1, rtol=1e-13, atol=0)                      # rotations keep norms
+    # pair 0 turns by pos radians; pair 16 by pos / sqrt(base); (1, 0) -> (cos, sin)
+    e = np.zeros(128)
+    e[64] = 1.0
+    e[64 + 32] = 1.0
+    r = orc.rope_last64(e, 3, base)
+    assert math.isclose(r[64], math.cos(3.0), abs_tol=1e-15) and math.isclose(r[65], math.sin(3.0), abs_tol=1e-15)
+    a16 = 3.0 / math.sqrt(base)
+    assert math.isclose(r[96], math.cos(a16), abs_tol=1e-15) and math.isclose(r[97], math.sin(a16), abs_tol=1e-15)
+    e2 = np.zeros(128)
+    e2[65] = 1.0                                                        # (0, 1) -> (-sin, cos)
+    r2 = orc.rope_last64(e2, 3, base)
+    assert math.isclose(r2[64], -math.sin(3.0), abs_tol=1e-15) and math.isclose(r2[65], math.cos(3.0), abs_tol=1e-15)
+    # composition: positions add
+    ab = orc.rope_last64(orc.rope_last64(row, 700, base), 41, base)
+    assert np.allclose(ab, orc.rope_last64(row, 741, base), rtol=0, atol=1e-12)
+
+
+def _bits(x):
+    return orc.bf16_round_rne(np.asarray(x, dtype=np.float64))
+
+
+def test_cache_write_row_bf16_and_fp8():
+    rng = np.random.default_rng(8)
+    row = _bits(rng.standard_normal(576) * 0.5)
+    stored, s, exact = orc.cache_write_row(row, 777, 10000.0, "bf16")
+    assert s is None and np.array_equal(stored[:512], row[:512])         # copies are exact
+    assert np.array_equal(stored, orc.bf16_round_rne(exact))
+    codes, s, exact = orc.cache_write_row(row, 777, 10000.0, "fp8_e4m3")
+    x32 = exact.astype(np.float32)
+    assert s == np.float32(np.abs(x32).max() / np.float32(448.0))
+    j = int(np.argmax(np.abs(x32)))
+    assert codes[j] in (0x7E, 0xFE)                                      # the row's max -> +-448
+    deq = orc.e4m3_code_to_f64(codes) * float(s)
+    pos = orc.e4m3_code_to_f64(np.arange(127, dtype=np.uint8))
+    step = np.diff(pos)[np.clip(np.searchsorted(pos, np.abs(x32 / s)) - 1, 0, 125)] * float(s)
+    assert np.all(np.abs(deq - x32) <= step / 2 * (1 + 1e-6))            # nearest code
+    z, sz, _ = orc.cache_write_row(np.zeros(128, dtype=np.uint16), 5, 10000.0, "fp8_e4m3")
+    assert sz == np.float32(1.0) and np.all((z & 0x7F) == 0)            # +-0 codes only
