@@ -215,6 +215,47 @@ def test_sparse_mla_alone(cfg):
             assert eo <= (2e-3 if cfg == 1 else 5e-3) and el <= 1e-4, (S, r, eo, el)
 
 
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_sparse_mla_running_max_moves(cfg):
+    """Selected rows scaled by 1, 10 and 30 tile by tile (64 tokens, in list
+    order): every head's maximum logit jumps by several nats from one tile to
+    the next, so the kernel must move its running maxima and rescale the
+    accumulated output (the lazy rule moves a maximum only past 2^8)."""
+    from workloads.synth import to_bf16_bits
+    wl = make_workload(config_spec(cfg, B=2, L=3000))
+    rng = np.random.default_rng(11)
+    k = 2048
+    idx = np.zeros((wl.R, k), np.int32)
+    cnt = np.zeros(wl.R, np.int32)
+    c = wl.kv
+    for r in range(wl.R):
+        b = int(wl.row_req[r])
+        n = min(k, int(wl.row_pos[r]) + 1)
+        sel = rng.choice(int(wl.row_pos[r]) + 1, n, replace=False).astype(np.int32)
+        idx[r, :n] = sel
+        cnt[r] = n
+        for rank, t in enumerate(sel):
+            f = (1.0, 10.0, 30.0)[(rank // 64) % 3]
+            pg, sl = c.physical_page(b, int(t) // c.page_size), int(t) % c.page_size
+            c.data[pg, sl] = to_bf16_bits(orc.bf16_bits_to_f64(c.data[pg, sl]) * f)
+    dw = upload(wl, DEV)
+    t_ = lambda a: torch.from_numpy(a).to(DEV)  # noqa: E731
+    for S in (1, 3):
+        out = torch.zeros((wl.R, wl.H, 512), device=DEV)
+        lse = torch.zeros((wl.R, wl.H), device=DEV)
+        ws = torch.zeros(max(api.dsa_sparse_mla_decode_workspace_size(wl.R, wl.H, k, S), 1),
+                         dtype=torch.uint8, device=DEV)
+        err = _err()
+        api.dsa_sparse_mla_decode(dw.q, wl.sm_scale, dw.kv, dw.rows, t_(idx), t_(cnt), out, lse,
+                                  err, workspace=ws, num_splits=S)
+        assert api.dsa_read_error(err) == 0
+        for r in range(wl.R):
+            O_ref, l_ref = orc.row_attention(wl, r, idx[r, : cnt[r]])
+            assert l_ref.max() > 10.0, "the scaled tiles dominate"
+            eo, el = attn_err(out[r].cpu().numpy(), lse[r].cpu().numpy(), O_ref, l_ref)
+            assert eo <= 2e-3 and el <= 1e-4, (S, r, eo, el)
+
+
 def test_lse_merge_against_oracle():
     rng = np.random.default_rng(4)
     P, R, H, dv = 5, 3, 4, 512
