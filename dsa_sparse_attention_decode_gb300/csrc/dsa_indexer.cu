@@ -5,7 +5,7 @@
 // shard) gets an indexer score before the top-2048 selection.  Score of token
 // t for query row r: sum_h w[r][h] * relu(q[r][h] . k[t]) over 64 heads x 128.
 //
-// Design (one persistent CTA per SM, 8 warps):
+// Design (one persistent CTA per SM, 8 or 12 warps):
 //   warp 0      TMA producer: 128-token tiles of the paged index-K cache,
 //               two 64-token page halves per tile, into a ring of stages.
 //   warp 1      tcgen05 issuer: D[128 tokens x 64*rows] = K_tile . Q^T with
@@ -18,11 +18,13 @@
 //               holds the rounding remainder of hi; together they keep every
 //               bf16 digit down to 2^-9 at that scale) that accumulate into
 //               the same TMEM columns; 2^-e goes into the head weight.
-//   warps 4-7   epilogue: one thread per token row of the tile reads its
+//   warps 4-7   epilogue (and warps 8-11, a second set, for fp8 keys or
+//               several rows per request: then each set takes one of the two
+//               accumulator slots): one thread per token row of the tile reads its
 //               TMEM lane, applies relu, the head weights (and the fp8
 //               per-token scale, read from the key stage, which is released
-//               only once the MMA and the four epilogue warps are done with
-//               it) and stores the fp32 score.
+//               only once the MMA and both epilogue sets are done with it)
+//               and stores the fp32 score.
 // Work units are (shard, request, tile); the flattened unit list is split
 // evenly over the CTAs.  All rows of a request share one key stream.
 #include <cuda_fp16.h>
@@ -35,7 +37,8 @@ namespace dsa {
 namespace {
 
 constexpr int kTileT = 128;
-constexpr int kThreads = 256;
+// 4 warps (producer, issuer, Q staging) + 4 epilogue warps per epilogue set
+__host__ __device__ constexpr int threads_of(int sets) { return 128 + 128 * sets; }
 constexpr int kOpBytes = kTileT * kIdxDim * 2;     // 32 KB bf16 key tile
 constexpr int kRawFp8Bytes = kTileT * kIdxDim;     // 16 KB e4m3 key tile
 // an fp8 stage: the e4m3 tile, then the (page, slot) of its two 64-token
@@ -178,9 +181,10 @@ __device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uin
   lo = static_cast<uint32_t>(l);
 }
 
-template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kFp8, int kSets>
+__global__ void __launch_bounds__(threads_of(kSets), 1)
     indexer_kernel(const __grid_constant__ IndexerLaunch P, const Layout L) {
+  constexpr int kThreads = threads_of(kSets);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -199,21 +203,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 32);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 33);
   int* s_start = reinterpret_cast<int*>(bars + 34);   // [pair, tile, nunits]
-  int* s_scan = reinterpret_cast<int*>(bars + 36);    // 8 warp sums
+  int* s_scan = reinterpret_cast<int*>(bars + 36);    // 12 warp sums
   PairMeta* meta = reinterpret_cast<PairMeta*>(sbase + L.off_meta);
 
   if (tid == 0) {
     for (int s = 0; s < L.stages; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
-      // released by the four epilogue warps once the tile's last
-      // accumulator has landed (its MMAs, which read the stage, are done)
-      mbar_init(bar(B_KEMPTY + s), 4);
+      // released by lane 0 of each epilogue warp, once each set
+      // has seen the accumulators of its chunks of the tile land (the MMAs,
+      // which read the stage, are then done)
+      mbar_init(bar(B_KEMPTY + s), 4 * kSets);
     }
     for (int o = 0; o < 2; ++o) {
       mbar_init(bar(B_ACCFULL + o), 1);
       mbar_init(bar(B_ACCEMPTY + o), 128);
       mbar_init(bar(B_PFULL + o), 1);
-      mbar_init(bar(B_PEMPTY + o), 128);
+      mbar_init(bar(B_PEMPTY + o), 128 * kSets);
     }
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
@@ -527,9 +532,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         wk.next(P);
       }
     } else {
-      // ------------------------------------------------ epilogue (warps 4..7)
-      const int et = tid - 128;            // token row of the tile / TMEM lane
+      // ------------------------------------------------ epilogue (warps 4..)
+      // With two sets of four warps each takes one accumulator slot: set 0
+      // (warps 4..7) the chunks that land in slot 0, set 1 (warps 8..11)
+      // those in slot 1, so two chunks are summed at once.
+      const int et = (tid - 128) & 127;    // token row of the tile / TMEM lane
       const int q4 = warp & 3;             // TMEM lane quarter of this warp
+      const int eset = (warp - 4) >> 2;    // the accumulator slot this set reads
       Walker wk;
       wk.start(P, start_pair, start_tile);
       uint32_t acc_iter = 0;
@@ -548,12 +557,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const PairMeta& m = meta[pair_j & 1];
         const int sl = wk.pair / P.num_reqs;
         const int t = wk.tile * kTileT + et;
+        // With two sets both wait for the tile's keys, also the set without
+        // a chunk in it: its release of the stage must not run ahead of the
+        // fill (it would count towards the stage's previous use).
+        if (kFp8 || kSets == 2) {
+          const bool got = mbar_wait(bar(B_KFULL + stage), phase, abort_flag);
+          if (!__all_sync(0xffffffffu, got)) break;
+        }
         float kscale = 1.0f;
         if (kFp8) {
           // the token's scale, from the (page, slot) the producer left behind
           // the keys; loaded now, used after the accumulator wait
-          const bool got = mbar_wait(bar(B_KFULL + stage), phase, abort_flag);
-          if (!__all_sync(0xffffffffu, got)) break;
           const int* where = reinterpret_cast<const int*>(sbase + L.off_ring +
                                                           stage * L.stage_bytes + kRawFp8Bytes);
           const int h = et >> 6;
@@ -570,6 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int rows_c = min(rpc, nr - c0);
           const int slot = static_cast<int>(acc_iter & 1u);
           const uint32_t aph = (acc_iter >> 1) & 1u;
+          if (kSets == 2 && slot != eset) {  // the other set's chunk
+            ++acc_iter;
+            continue;
+          }
           if (!mbar_wait(bar(B_ACCFULL + slot), aph, abort_flag)) {
             ok = false;
             break;
@@ -625,6 +643,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+template <bool kFp8, int kSets>
+cudaError_t launch_one(const IndexerLaunch& p, const Layout& L, int grid, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(indexer_kernel<kFp8, kSets>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if (e != cudaSuccess) return e;
+  indexer_kernel<kFp8, kSets><<<grid, threads_of(kSets), L.total, stream>>>(p, L);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_indexer(const IndexerLaunch& p, cudaStream_t stream) {
@@ -632,19 +660,13 @@ cudaError_t launch_indexer(const IndexerLaunch& p, cudaStream_t stream) {
   if (L.stages < 2) return cudaErrorInvalidValue;
   int grid = num_sms();
   if (grid <= 0) return cudaErrorInvalidDevice;
-  cudaError_t e;
-  if (p.fp8) {
-    e = cudaFuncSetAttribute(indexer_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L.total);
-    if (e != cudaSuccess) return e;
-    indexer_kernel<true><<<grid, kThreads, L.total, stream>>>(p, L);
-  } else {
-    e = cudaFuncSetAttribute(indexer_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L.total);
-    if (e != cudaSuccess) return e;
-    indexer_kernel<false><<<grid, kThreads, L.total, stream>>>(p, L);
-  }
-  return cudaGetLastError();
+  // A second epilogue set pays off where the epilogue carries weight: fp8
+  // keys (a scale load per token, half the key bytes per tile) or several
+  // rows per request; for one bf16 row the MMA issue is the bound and the
+  // extra warps only crowd the issuing thread's sub-partition.
+  if (p.fp8) return launch_one<true, 2>(p, L, grid, stream);
+  if (p.max_rows > 1) return launch_one<false, 2>(p, L, grid, stream);
+  return launch_one<false, 1>(p, L, grid, stream);
 }
 
 }  // namespace dsa

@@ -188,6 +188,12 @@ __global__ void __launch_bounds__(kMergeThreads, 1) shard_topk_merge_kernel(cons
 // lse = ln sum_p exp(lse_p), out = sum_p exp(lse_p - lse) O_p; parts whose
 // lse is -inf hold no tokens and are not read.  One CTA per (row, head), one
 // float4 of the value vector per thread.
+// One CTA per (row, head), one float4 of the value dims per thread.  Up to
+// kFastParts partials, every load (LSEs and partial outputs alike) is issued
+// before any is used, so the kernel waits for one round trip to L2; an
+// empty partial (LSE -inf, output not written) is skipped by selection.
+constexpr int kFastParts = 8;
+
 __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
                                  const float* __restrict__ lse_parts, int parts, int rows,
                                  int heads, int dv, float* __restrict__ out,
@@ -196,30 +202,59 @@ __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
   pdl_trigger();
   pdl_wait();  // the partials come from the previous grid
   const long long stride_p = static_cast<long long>(rows) * heads;
-  float m = -__int_as_float(0x7f800000);
-  for (int p = 0; p < parts; ++p) m = fmaxf(m, __ldcg(lse_parts + p * stride_p + rh));
-  const bool empty = (m == -__int_as_float(0x7f800000));
-  float den = 0.0f;
-  if (!empty)
-    for (int p = 0; p < parts; ++p) den += expf(__ldcg(lse_parts + p * stride_p + rh) - m);
-  const float inv = empty ? 0.0f : 1.0f / den;
-  for (int d4 = threadIdx.x; d4 < dv / 4; d4 += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (!empty) {
-      for (int p = 0; p < parts; ++p) {
-        const float l = __ldcg(lse_parts + p * stride_p + rh);
-        if (l == -__int_as_float(0x7f800000)) continue;
-        const float wgt = expf(l - m) * inv;
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(O_parts + (p * stride_p + rh) * dv) + d4);
-        acc.x = fmaf(wgt, v.x, acc.x);
-        acc.y = fmaf(wgt, v.y, acc.y);
-        acc.z = fmaf(wgt, v.z, acc.z);
-        acc.w = fmaf(wgt, v.w, acc.w);
+  const int d4 = threadIdx.x;
+  const bool has_d = d4 < dv / 4;
+  const float kNegInf = -__int_as_float(0x7f800000);
+  float m = kNegInf, den = 0.0f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (parts <= kFastParts) {
+    float l[kFastParts];
+    float4 v[kFastParts];
+#pragma unroll
+    for (int p = 0; p < kFastParts; ++p) {
+      l[p] = p < parts ? __ldcg(lse_parts + p * stride_p + rh) : kNegInf;
+      v[p] = (p < parts && has_d)
+                 ? __ldcg(reinterpret_cast<const float4*>(O_parts + (p * stride_p + rh) * dv) + d4)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int p = 0; p < kFastParts; ++p) m = fmaxf(m, l[p]);
+    if (m != kNegInf) {
+#pragma unroll
+      for (int p = 0; p < kFastParts; ++p) {
+        const bool live = l[p] != kNegInf;
+        const float e = live ? expf(l[p] - m) : 0.0f;
+        den += e;
+        acc.x = live ? fmaf(e, v[p].x, acc.x) : acc.x;
+        acc.y = live ? fmaf(e, v[p].y, acc.y) : acc.y;
+        acc.z = live ? fmaf(e, v[p].z, acc.z) : acc.z;
+        acc.w = live ? fmaf(e, v[p].w, acc.w) : acc.w;
       }
     }
-    reinterpret_cast<float4*>(out + static_cast<long long>(rh) * dv)[d4] = acc;
+  } else {
+    for (int p = 0; p < parts; ++p) m = fmaxf(m, __ldcg(lse_parts + p * stride_p + rh));
+    if (m != kNegInf) {
+      for (int p = 0; p < parts; ++p) {
+        const float l = __ldcg(lse_parts + p * stride_p + rh);
+        if (l == kNegInf) continue;
+        const float e = expf(l - m);
+        den += e;
+        if (has_d) {
+          const float4 v =
+              __ldcg(reinterpret_cast<const float4*>(O_parts + (p * stride_p + rh) * dv) + d4);
+          acc.x = fmaf(e, v.x, acc.x);
+          acc.y = fmaf(e, v.y, acc.y);
+          acc.z = fmaf(e, v.z, acc.z);
+          acc.w = fmaf(e, v.w, acc.w);
+        }
+      }
+    }
   }
-  if (threadIdx.x == 0) out_lse[rh] = empty ? m : m + logf(den);
+  const float inv = m == kNegInf ? 0.0f : 1.0f / den;
+  if (has_d)
+    reinterpret_cast<float4*>(out + static_cast<long long>(rh) * dv)[d4] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (threadIdx.x == 0) out_lse[rh] = m == kNegInf ? m : m + logf(den);
 }
 
 }  // namespace
@@ -240,7 +275,8 @@ cudaError_t launch_lse_merge(const float* O_parts, const float* lse_parts, int p
                              int heads, int dv, float* out, float* out_lse, cudaStream_t stream,
                              bool pdl) {
   if (rows * heads == 0) return cudaSuccess;
-  const int threads = dv / 4 >= 128 ? 128 : ((dv / 4 + 31) / 32) * 32;
+  if (dv % 4 != 0 || dv / 4 > 1024) return cudaErrorInvalidValue;
+  const int threads = ((dv / 4 + 31) / 32) * 32;  // one float4 of the value dims per thread
   return launch_ex(lse_merge_kernel, dim3(rows * heads), dim3(threads), 0, stream, pdl, O_parts,
                    lse_parts, parts, rows, heads, dv, out, out_lse);
 }
