@@ -56,6 +56,9 @@ def parse():
                     help="time the fused step on configuration 0..4 instead (device time only, "
                          "one JSON line; the contract line is the default configuration 1)")
     ap.add_argument("--batch", type=int, default=None, help="requests of configuration 4")
+    ap.add_argument("--rows-per-req", type=int, default=None,
+                    help="with --config: query rows per request at consecutive positions "
+                         "(MTP verify or a multi-query extend)")
     ap.add_argument("--kernel", default=None, choices=["indexer", "topk", "mla", "cache_write"],
                     help="time one kernel of the step alone on the same workload (a short "
                          "run for profilers: W warm-up launches, then K timed ones)")
@@ -231,6 +234,8 @@ def run_config(args):
     pkg.lib()
     dev = torch.device("cuda", 0)
     kw = {"B": args.batch} if (args.config == 4 and args.batch) else {}
+    if args.rows_per_req:
+        kw["rows_per_req"] = args.rows_per_req
     spec = config_spec(args.config, **kw)
     wl = make_workload(spec)
     dw = upload(wl, dev, shards=spec.shards > 1, unsharded=spec.shards == 1)
@@ -261,7 +266,7 @@ def run_config(args):
     peaks, kind = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     gbs = (idx_b + mla_b) / sec / 1e9
-    print(json.dumps({"config": spec.name, "rows": R, "shards": spec.shards,
+    print(json.dumps({"config": spec.name, "rows": R, "rows_per_req": spec.rows_per_req, "shards": spec.shards,
                       "ms_per_step": round(sec * 1e3, 4), "rows_per_s": round(R / sec, 1),
                       "algorithmic_bytes": idx_b + mla_b, "path_gbs": round(gbs, 1),
                       "path_frac_of_measured": round(gbs / hbm, 4), "peak_source": kind}),

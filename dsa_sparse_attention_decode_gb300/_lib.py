@@ -26,6 +26,7 @@ DSA_DEVERR_GROUP = 1 << 6
 
 DSA_DTYPE_BF16 = 0
 DSA_DTYPE_FP8_E4M3 = 1
+DSA_MAX_ROWS_PER_REQ = 1024
 
 INDEX_HEADS = 64
 INDEX_DIM = 128

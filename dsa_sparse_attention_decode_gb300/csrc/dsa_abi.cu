@@ -64,7 +64,7 @@ int check_rows(const dsa_rows* rw) {
   if (rw == nullptr) return DSA_ERR_INVALID_ARG;
   if (rw->num_rows < 0 || rw->num_reqs < 1 || rw->max_len < 1) return DSA_ERR_INVALID_ARG;
   if (rw->max_rows_per_req < 1) return DSA_ERR_INVALID_ARG;
-  if (rw->max_rows_per_req > kMaxRowsPerReq) return DSA_ERR_UNSUPPORTED;
+  if (rw->max_rows_per_req > DSA_MAX_ROWS_PER_REQ) return DSA_ERR_UNSUPPORTED;
   if (rw->num_rows > 0 && (rw->row_start == nullptr || rw->row_pos == nullptr))
     return DSA_ERR_INVALID_ARG;
   return DSA_OK;
@@ -83,6 +83,14 @@ int resolve_splits(int num_splits, int work_rows, int k, int expected) {
 int split_chunk(int splits, int k) {
   int chunk = (k + splits - 1) / splits;
   return (chunk + 63) / 64 * 64;
+}
+
+// The rows of a request are scored in groups of at most kRowsPerGroup
+// (the query rows one CTA holds in shared memory); each group streams the
+// request's keys once.
+void set_row_groups(IndexerLaunch& L, int max_rows_per_req) {
+  L.max_rows = max_rows_per_req < kRowsPerGroup ? max_rows_per_req : kRowsPerGroup;
+  L.groups = (max_rows_per_req + kRowsPerGroup - 1) / kRowsPerGroup;
 }
 
 void fill_indexer_shard(IndexerLaunch& L, int i, const dsa_paged_cache& c) {
@@ -180,7 +188,7 @@ int dsa_indexer_scores(const uint16_t* q_idx, const float* w_idx, const dsa_page
   L.row_pos = rows->row_pos;
   L.num_rows = rows->num_rows;
   L.num_reqs = rows->num_reqs;
-  L.max_rows = rows->max_rows_per_req;
+  set_row_groups(L, rows->max_rows_per_req);
   L.scores = scores;
   L.ld = ld_scores;
   L.shard_stride = 0;
@@ -477,7 +485,7 @@ int dsa_decode(const dsa_decode_desc* d, void* workspace, size_t workspace_bytes
     L.row_pos = d->rows.row_pos;
     L.num_rows = R;
     L.num_reqs = d->rows.num_reqs;
-    L.max_rows = d->rows.max_rows_per_req;
+    set_row_groups(L, d->rows.max_rows_per_req);
     L.scores = reinterpret_cast<float*>(ws + lay.scores);
     L.ld = lay.ld_scores;
     L.shard_stride = static_cast<int64_t>(R) * lay.ld_scores;

@@ -17,7 +17,7 @@ constexpr int kIdxDim = DSA_INDEX_DIM;
 constexpr int kKvDim = DSA_KV_DIM;
 constexpr int kVDim = DSA_V_DIM;
 constexpr int kMaxShards = DSA_MAX_SHARDS;
-constexpr int kMaxRowsPerReq = 8;
+constexpr int kRowsPerGroup = 8;  // indexer query rows one CTA holds at a time
 
 // A bounded on-chip wait gives up after this long (ns of %globaltimer).  Every
 // kernel here finishes in well under a millisecond, so reaching it means the

@@ -49,9 +49,9 @@ constexpr int kHalfBf16Box = 64 * 64 * 2;          // one TMA box: 64 tokens x 6
 constexpr int kSmemLimit = 227 * 1024;
 
 struct PairMeta {           // per (shard, request) pair, written by the aux warps
-  float w[kMaxRowsPerReq][kIdxHeads];
-  int valid[kMaxRowsPerReq];
-  int row[kMaxRowsPerReq];
+  float w[kRowsPerGroup][kIdxHeads];
+  int valid[kRowsPerGroup];
+  int row[kRowsPerGroup];
 };
 
 struct Layout {
@@ -101,21 +101,35 @@ struct PairInfo {
   int row0, nr, len, ntiles;
 };
 
+// A work pair is (shard cache, request, row group): the rows of a request
+// form groups of at most max_rows consecutive rows (the query rows one CTA
+// holds in shared memory), and every group streams the request's keys.
+__device__ __forceinline__ int pair_shard(const IndexerLaunch& P, int pair) {
+  return pair / (P.num_reqs * P.groups);
+}
+__device__ __forceinline__ int pair_req(const IndexerLaunch& P, int pair) {
+  return (pair / P.groups) % P.num_reqs;
+}
+
 __device__ PairInfo pair_info(const IndexerLaunch& P, int pair, bool report) {
-  const int sl = pair / P.num_reqs;
-  const int b = pair - sl * P.num_reqs;
+  const int sl = pair_shard(P, pair);
+  const int b = pair_req(P, pair);
+  const int g = pair % P.groups;
   const int shard = P.shard_base + sl;
   PairInfo pi{0, 0, 0, 0};
-  const int r0 = __ldg(P.row_start + b);
-  const int r1 = __ldg(P.row_start + b + 1);
-  if (r0 < 0 || r1 < r0 || r1 > P.num_rows) {
+  const int q0 = __ldg(P.row_start + b);
+  const int q1 = __ldg(P.row_start + b + 1);
+  if (q0 < 0 || q1 < q0 || q1 > P.num_rows) {
     if (report) raise_err(P.d_err, DSA_DEVERR_ROWS);
     return pi;
   }
-  if (r1 - r0 > P.max_rows) {
-    if (report) raise_err(P.d_err, DSA_DEVERR_GROUP);
+  if (q1 - q0 > P.max_rows * P.groups) {
+    if (report && g == 0) raise_err(P.d_err, DSA_DEVERR_GROUP);
     return pi;
   }
+  const int r0 = q0 + g * P.max_rows;
+  const int r1 = min(q1, r0 + P.max_rows);
+  if (r0 >= r1) return pi;  // the request has fewer groups
   int len = 0;
   for (int r = r0; r < r1; ++r) {
     const int pos = __ldg(P.row_pos + r);
@@ -145,7 +159,7 @@ struct Walker {
   __device__ void start(const IndexerLaunch& P, int p, int t) {
     pair = p;
     tile = t;
-    npairs = P.nshards * P.num_reqs;
+    npairs = P.nshards * P.num_reqs * P.groups;
     pi = pair_info(P, pair, false);
     skip(P);
   }
@@ -237,7 +251,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
   pdl_wait();  // inputs may come from the previous grid
 
   // ---- schedule: count units of every (shard, request) pair, split evenly
-  const int npairs = P.nshards * P.num_reqs;
+  const int npairs = P.nshards * P.num_reqs * P.groups;
   {
     const int chunk = (npairs + kThreads - 1) / kThreads;
     const int p0 = min(npairs, tid * chunk);
@@ -297,8 +311,8 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
         for (int u = 0; u < nunits; ++u) {
           if (!mbar_wait(bar(B_KEMPTY + stage), phase ^ 1u, abort_flag)) break;
           ++issued;
-          const int sl = wk.pair / P.num_reqs;
-          const int b = wk.pair - sl * P.num_reqs;
+          const int sl = pair_shard(P, wk.pair);
+          const int b = pair_req(P, wk.pair);
           int pages[2] = {-1, -1}, slots[2] = {0, 0};
           uint32_t bytes = 0;
           for (int h = 0; h < 2; ++h) {
@@ -446,7 +460,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
                            abort_flag);
           if (ok && pair_j >= 1)
             ok = mbar_wait(bar(B_QEMPTY), static_cast<uint32_t>(pair_j - 1) & 1u, abort_flag);
-          const int sl = wk.pair / P.num_reqs;
+          const int sl = pair_shard(P, wk.pair);
           const int shard = P.shard_base + sl;
           const int nr = wk.pi.nr;
           const int row0 = wk.pi.row0;
@@ -555,7 +569,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
           if (!__all_sync(0xffffffffu, got)) break;
         }
         const PairMeta& m = meta[pair_j & 1];
-        const int sl = wk.pair / P.num_reqs;
+        const int sl = pair_shard(P, wk.pair);
         const int t = wk.tile * kTileT + et;
         // With two sets both wait for the tile's keys, also the set without
         // a chunk in it: its release of the stage must not run ahead of the

@@ -31,7 +31,8 @@ struct IndexerLaunch {
   const int32_t* row_pos;
   int32_t num_rows;
   int32_t num_reqs;
-  int32_t max_rows;     // rows per request bound (1..8)
+  int32_t max_rows;     // rows per group (1..8): query rows one CTA holds at a time
+  int32_t groups;       // row groups per request (rows per request <= max_rows * groups)
   float* scores;        // cache i writes rows at scores + i * shard_stride
   int64_t ld;
   int64_t shard_stride;

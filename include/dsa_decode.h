@@ -76,6 +76,7 @@ extern "C" {
 #define DSA_KV_DIM 576       /* MLA latent row width (512 value + 64 rope) */
 #define DSA_V_DIM 512        /* value width */
 #define DSA_MAX_SHARDS 8     /* token shards of the emulated DCP group */
+#define DSA_MAX_ROWS_PER_REQ 1024 /* query rows of one request (MTP, multi-query extend) */
 
 /* status codes returned by every entry point */
 enum {
@@ -134,7 +135,10 @@ typedef struct {
  *               = 0, row_start[num_reqs] = num_rows);
  *   row_pos:    device [num_rows], position of each row's query; the row sees
  *               tokens 0..row_pos[r] of its request;
- *   max_rows_per_req: host bound on rows of one request (1..8);
+ *   max_rows_per_req: host bound on rows of one request
+ *               (1..DSA_MAX_ROWS_PER_REQ); the indexer scores a request's
+ *               rows in groups of up to 8, each group streaming the
+ *               request's keys once;
  *   max_len:    host bound with row_pos[r] < max_len for every row; sizes the
  *               score rows and the workspace.
  * Several rows of one request (MTP / EAGLE verify: one row per draft token)
@@ -180,7 +184,8 @@ int dsa_read_error(const int32_t* d_err, int32_t* h_err, void* stream);
  *
  * Errors: DSA_ERR_INVALID_ARG for NULL pointers, bad sizes, a cache that is
  * not 128 wide, ld_scores too small; DSA_ERR_UNSUPPORTED for
- * max_rows_per_req > 8.  Device: DSA_DEVERR_ROWS/POS/PAGE/GROUP.
+ * max_rows_per_req > DSA_MAX_ROWS_PER_REQ.  Device: DSA_DEVERR_ROWS/POS/PAGE/GROUP
+ * (GROUP: a request with more than max_rows_per_req rows).
  */
 int dsa_indexer_scores(const uint16_t* q_idx, const float* w_idx,
                        const dsa_paged_cache* idx_k, const dsa_rows* rows,

@@ -79,7 +79,7 @@ def test_host_validation_rejects_bad_arguments(lib):
         ctypes.c_void_p(16), 16, err, None)
     assert st == C.DSA_ERR_INVALID_ARG
     # more rows per request than supported
-    rows.max_rows_per_req = 9
+    rows.max_rows_per_req = C.DSA_MAX_ROWS_PER_REQ + 1
     st = lib.dsa_indexer_scores(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.byref(
         C.DsaPagedCache(data=16, scale=None, block_table=None, dtype=0, row_elems=128,
                         page_size=64, num_pages=4, max_blocks=4)), ctypes.byref(rows), 0, 1,

@@ -47,6 +47,31 @@ def test_config4_reduced_ragged_fp8():
     _run(config_spec(4, B=9, L_lo=300, L_hi=12000))
 
 
+@pytest.mark.parametrize("rpr,dtype", [(9, "bf16"), (20, "fp8_e4m3"), (33, "bf16")])
+def test_multi_query_extend_rows(rpr, dtype):
+    """More query rows per request than one indexer row group (8) holds, at
+    consecutive positions (a multi-query extend): the rows are scored in
+    groups of 8 that each stream the request's keys, and every row keeps its
+    own causal window, top-k and attention."""
+    _run(config_spec(2, B=2, L_lo=2500, L_hi=5000, rows_per_req=rpr, dtype=dtype))
+
+
+def test_multi_query_extend_rows_sharded():
+    _run(config_spec(3, B=2, L=3001, shards=2, rows_per_req=12), sharded=True)
+
+
+def test_more_rows_than_declared_sets_error_bit():
+    import dataclasses
+
+    from dsa_sparse_attention_decode_gb300 import _lib as C
+    wl = make_workload(config_spec(2, B=2, L_lo=2500, L_hi=3000, rows_per_req=20,
+                                   dtype="bf16"))
+    dw = upload(wl, "cuda")
+    dw.rows = dataclasses.replace(dw.rows, max_rows_per_req=16)  # two groups of 8 < 20 rows
+    run = DecodeRun(dw)
+    assert run.run() & C.DSA_DEVERR_GROUP
+
+
 @pytest.mark.parametrize("S", [1, 2, 7, 32])
 def test_split_counts_agree(S):
     _run(config_spec(1, B=2, L=4500), num_splits=S)
