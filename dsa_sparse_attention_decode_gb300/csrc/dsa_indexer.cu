@@ -59,7 +59,8 @@ struct Layout {
   int stage_bytes;
   int q_rows;      // max_rows * 64
   int q_kb_stride; // bytes between the two 64-dim halves of Q
-  int off_ring, off_q, off_meta, off_bar, total;
+  int off_ring, off_q, off_meta, off_rows, off_bar, total;
+  int rows_smem;   // row_start and row_pos copied to shared memory (they fit)
   int slot_cols, tmem_cols, rows_per_chunk;
 };
 
@@ -68,8 +69,14 @@ __host__ __device__ inline int rows_per_chunk_of(int nr) {
   return (nr + nch - 1) / nch;
 }
 
-__host__ inline Layout make_layout(int fp8, int max_rows) {
+// row_ints: num_reqs + 1 + num_rows, the row metadata a CTA copies to
+// shared memory for its schedule when it fits in kRowsSmemCap bytes.
+constexpr int kRowsSmemCap = 8192;
+
+__host__ inline Layout make_layout(int fp8, int max_rows, int row_ints) {
   Layout L{};
+  L.rows_smem = row_ints * 4 <= kRowsSmemCap;
+  const int rows_bytes = L.rows_smem ? (row_ints * 4 + 15) / 16 * 16 : 0;
   L.q_rows = max_rows * kIdxHeads;
   L.q_kb_stride = L.q_rows * 128;
   L.rows_per_chunk = rows_per_chunk_of(max_rows);
@@ -80,7 +87,7 @@ __host__ inline Layout make_layout(int fp8, int max_rows) {
   const int q_bytes = 2 * L.q_kb_stride;
   const int meta_bytes = 2 * static_cast<int>(sizeof(PairMeta));
   const int bar_bytes = 512;
-  const int fixed = 1024 /*align*/ + q_bytes + meta_bytes + bar_bytes;
+  const int fixed = 1024 /*align*/ + q_bytes + meta_bytes + rows_bytes + bar_bytes;
   L.stage_bytes = fp8 ? kFp8StageBytes : kOpBytes;
   L.stages = (kSmemLimit - fixed) / L.stage_bytes;
   if (L.stages > 8) L.stages = 8;
@@ -91,6 +98,8 @@ __host__ inline Layout make_layout(int fp8, int max_rows) {
   off += q_bytes;
   L.off_meta = off;
   off += meta_bytes;
+  L.off_rows = off;
+  off += rows_bytes;
   L.off_bar = off;
   off += bar_bytes;
   L.total = off + 1024;
@@ -111,14 +120,27 @@ __device__ __forceinline__ int pair_req(const IndexerLaunch& P, int pair) {
   return (pair / P.groups) % P.num_reqs;
 }
 
-__device__ PairInfo pair_info(const IndexerLaunch& P, int pair, bool report) {
+// The request's row range and the rows' positions, from the shared-memory
+// copy when the layout holds one.
+struct RowMeta {
+  const int* rs;  // row_start copy, or nullptr: read the global arrays
+  const int* rp;
+  __device__ int start(const IndexerLaunch& P, int b) const {
+    return rs ? rs[b] : __ldg(P.row_start + b);
+  }
+  __device__ int pos(const IndexerLaunch& P, int r) const {
+    return rs ? rp[r] : __ldg(P.row_pos + r);
+  }
+};
+
+__device__ PairInfo pair_info(const IndexerLaunch& P, const RowMeta& M, int pair, bool report) {
   const int sl = pair_shard(P, pair);
   const int b = pair_req(P, pair);
   const int g = pair % P.groups;
   const int shard = P.shard_base + sl;
   PairInfo pi{0, 0, 0, 0};
-  const int q0 = __ldg(P.row_start + b);
-  const int q1 = __ldg(P.row_start + b + 1);
+  const int q0 = M.start(P, b);
+  const int q1 = M.start(P, b + 1);
   if (q0 < 0 || q1 < q0 || q1 > P.num_rows) {
     if (report) raise_err(P.d_err, DSA_DEVERR_ROWS);
     return pi;
@@ -132,7 +154,7 @@ __device__ PairInfo pair_info(const IndexerLaunch& P, int pair, bool report) {
   if (r0 >= r1) return pi;  // the request has fewer groups
   int len = 0;
   for (int r = r0; r < r1; ++r) {
-    const int pos = __ldg(P.row_pos + r);
+    const int pos = M.pos(P, r);
     if (pos < 0) {
       if (report) raise_err(P.d_err, DSA_DEVERR_POS);
       return pi;
@@ -156,18 +178,20 @@ __device__ PairInfo pair_info(const IndexerLaunch& P, int pair, bool report) {
 struct Walker {
   int pair, tile, npairs;
   PairInfo pi;
-  __device__ void start(const IndexerLaunch& P, int p, int t) {
+  RowMeta M;
+  __device__ void start(const IndexerLaunch& P, const RowMeta& m, int p, int t) {
+    M = m;
     pair = p;
     tile = t;
     npairs = P.nshards * P.num_reqs * P.groups;
-    pi = pair_info(P, pair, false);
+    pi = pair_info(P, M, pair, false);
     skip(P);
   }
   __device__ void skip(const IndexerLaunch& P) {
     while (tile >= pi.ntiles && pair + 1 < npairs) {
       ++pair;
       tile = 0;
-      pi = pair_info(P, pair, false);
+      pi = pair_info(P, M, pair, false);
     }
   }
   __device__ void next(const IndexerLaunch& P) {
@@ -250,6 +274,34 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
 
   pdl_wait();  // inputs may come from the previous grid
 
+  // L2 prefetch of the block tables and the queries of this launch (each
+  // thread of the grid takes every n-th 128-byte line), so that the first
+  // tile's page lookups and the query staging find them in L2
+  {
+    const long long nthreads = static_cast<long long>(gridDim.x) * kThreads;
+    const long long first = static_cast<long long>(blockIdx.x) * kThreads + tid;
+    auto prefetch = [&](const void* base, long long bytes) {
+      for (long long off = first * 128; off < bytes; off += nthreads * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char*>(base) + off));
+    };
+    for (int i = 0; i < P.nshards; ++i)
+      if (P.block_table[i] != nullptr)
+        prefetch(P.block_table[i], static_cast<long long>(P.num_reqs) * P.max_blocks[i] * 4);
+    prefetch(P.q_idx, static_cast<long long>(P.num_rows) * kIdxHeads * kIdxDim * 2);
+    prefetch(P.w_idx, static_cast<long long>(P.num_rows) * kIdxHeads * 4);
+  }
+  // every request's row range and every row's position, in one round of
+  // loads (the schedule below would otherwise wait for two dependent ones)
+  RowMeta rm{nullptr, nullptr};
+  if (L.rows_smem) {
+    int* rs = reinterpret_cast<int*>(sbase + L.off_rows);
+    int* rp = rs + P.num_reqs + 1;
+    for (int i = tid; i <= P.num_reqs; i += kThreads) rs[i] = __ldg(P.row_start + i);
+    for (int i = tid; i < P.num_rows; i += kThreads) rp[i] = __ldg(P.row_pos + i);
+    __syncthreads();
+    rm = RowMeta{rs, rp};
+  }
+
   // ---- schedule: count units of every (shard, request) pair, split evenly
   const int npairs = P.nshards * P.num_reqs * P.groups;
   {
@@ -257,7 +309,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
     const int p0 = min(npairs, tid * chunk);
     const int p1 = min(npairs, p0 + chunk);
     int mine = 0;
-    for (int p = p0; p < p1; ++p) mine += pair_info(P, p, blockIdx.x == 0).ntiles;
+    for (int p = p0; p < p1; ++p) mine += pair_info(P, rm, p, blockIdx.x == 0).ntiles;
     int incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -278,7 +330,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
     if (u0 < u1 && excl <= u0 && u0 < excl + mine) {
       int acc = excl;
       for (int p = p0; p < p1; ++p) {
-        const int n = pair_info(P, p, false).ntiles;
+        const int n = pair_info(P, rm, p, false).ntiles;
         if (u0 < acc + n) {
           s_start[0] = p;
           s_start[1] = static_cast<int>(u0 - acc);
@@ -304,7 +356,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
       // ------------------------------------------------ TMA producer
       if (lane == 0) {
         Walker wk;
-        wk.start(P, start_pair, start_tile);
+        wk.start(P, rm, start_pair, start_tile);
         int stage = 0;
         uint32_t phase = 0;
         int issued = 0;
@@ -378,7 +430,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
       // ------------------------------------------------ MMA issuer
       if (lane == 0) {
         Walker wk;
-        wk.start(P, start_pair, start_tile);
+        wk.start(P, rm, start_pair, start_tile);
         int stage = 0;
         uint32_t phase = 0;
         uint32_t acc_iter = 0;
@@ -445,7 +497,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
       // ------------------------------------------------ Q staging
       const int at = tid - 64;  // 0..63
       Walker wk;
-      wk.start(P, start_pair, start_tile);
+      wk.start(P, rm, start_pair, start_tile);
       int pair_j = -1, last_pair = -1;
       // A failed (timed-out) wait stops the work of this thread but it keeps
       // passing the same named barriers as its partner warp.
@@ -554,7 +606,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
       const int q4 = warp & 3;             // TMEM lane quarter of this warp
       const int eset = (warp - 4) >> 2;    // the accumulator slot this set reads
       Walker wk;
-      wk.start(P, start_pair, start_tile);
+      wk.start(P, rm, start_pair, start_tile);
       uint32_t acc_iter = 0;
       int stage = 0;
       uint32_t phase = 0;
@@ -670,7 +722,7 @@ cudaError_t launch_one(const IndexerLaunch& p, const Layout& L, int grid, cudaSt
 }  // namespace
 
 cudaError_t launch_indexer(const IndexerLaunch& p, cudaStream_t stream) {
-  const Layout L = make_layout(p.fp8, p.max_rows);
+  const Layout L = make_layout(p.fp8, p.max_rows, p.num_reqs + 1 + p.num_rows);
   if (L.stages < 2) return cudaErrorInvalidValue;
   int grid = num_sms();
   if (grid <= 0) return cudaErrorInvalidDevice;

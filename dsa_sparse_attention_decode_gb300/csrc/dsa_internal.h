@@ -106,6 +106,7 @@ struct MlaLaunch {
   int32_t k;
   int32_t num_splits;      // S
   int32_t chunk;           // tokens per split (multiple of 64)
+  int32_t bt_smem;         // block-table entries cached in shared memory (set by the launcher)
   float* out;              // when parts == 1: [R][H][512]
   float* out_lse;
   float* part_out;         // else: part p = w * S + s at part_out + p*R*H*512

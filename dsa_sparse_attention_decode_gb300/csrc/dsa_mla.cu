@@ -39,11 +39,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct MlaSmem {
-  int off_q, off_kv, off_raw, off_p, off_red, off_kscale, off_misc, off_bar, total;
+  int off_q, off_kv, off_raw, off_p, off_red, off_kscale, off_misc, off_bt, off_bar, total;
   int kv_bufs;
 };
 
-__host__ __device__ inline MlaSmem mla_smem(int heads, int fp8, int chunk) {
+// bt_ints: entries of a request's block-table row kept in shared memory (0:
+// the gather reads the global table)
+__host__ __device__ inline MlaSmem mla_smem(int heads, int fp8, int chunk, int bt_ints = 0) {
   MlaSmem s{};
   int off = 0;
   s.off_q = off;
@@ -61,6 +63,8 @@ __host__ __device__ inline MlaSmem mla_smem(int heads, int fp8, int chunk) {
   off += fp8 ? chunk * 4 : 0;
   s.off_misc = off;
   off += 64 * 4 + heads * 4;
+  s.off_bt = off;
+  off += bt_ints * 4;
   off = (off + 15) & ~15;
   s.off_bar = off;  // mbarriers: full[2], empty[2], abort flag
   off += 64;
@@ -121,8 +125,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
   constexpr int NTW = MT;                // n8 token tiles per warp in S = q.kv^T
   constexpr int TGS = 8 / MT;            // token groups
   extern __shared__ __align__(16) uint8_t smem[];
-  const MlaSmem S = mla_smem(H, kFp8, P.chunk);
+  const MlaSmem S = mla_smem(H, kFp8, P.chunk, P.bt_smem);
   uint8_t* q_s = smem + S.off_q;
+  int* bt_s = reinterpret_cast<int*>(smem + S.off_bt);
   uint8_t* kv_s = smem + S.off_kv;
   uint8_t* raw_s = smem + S.off_raw;
   uint8_t* p_s = smem + S.off_p;
@@ -172,8 +177,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
   }
   __syncthreads();  // the request index and the barriers
   const int b = misc[0];
+  // the request's block-table row (an input the previous grid does not write)
+  const bool bt_smem = P.bt_smem > 0 && b >= 0 && P.block_table[w] != nullptr;
+  if (bt_smem) {
+    const int32_t* row = P.block_table[w] + static_cast<long long>(b) * P.max_blocks[w];
+    for (int j = tid; j < P.max_blocks[w]; j += kThreads) bt_s[j] = __ldg(row + j);
+  }
+  __syncthreads();
   pdl_wait();  // the selections come from the previous grid
 
+  // a gather thread's first selection is loaded together with the count
+  const int gt0 = tid - kCompute;
+  const int t_first = (warp >= kCompute / 32 && split * P.chunk + gt0 < P.k)
+                          ? __ldcg(P.idx + static_cast<long long>(qrow) * P.k + split * P.chunk + gt0)
+                          : -1;
   int cnt = __ldcg(P.count + qrow);
   if (cnt < 0 || cnt > P.k) {
     if (tid == 0) raise_err(P.d_err, DSA_DEVERR_INDEX);
@@ -219,14 +236,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
       ks = 0.0f;
       const int i = tile * kTile + gt;
       if (tile >= ntiles || i >= ntok) return;  // no row: zero-filled
-      const int t = __ldcg(ilist + i);
+      const int t = tile == 0 ? t_first : __ldcg(ilist + i);
       if (b < 0 || t < 0 || static_cast<long long>(t) >= span) {
         raise_err(P.d_err, DSA_DEVERR_INDEX);
         return;
       }
       const int lp = t / psz;
-      const int pg = bt ? __ldg(bt + static_cast<long long>(b) * P.max_blocks[w] + lp)
-                        : b * P.max_blocks[w] + lp;
+      const int pg = bt_smem ? bt_s[lp]
+                     : bt ? __ldg(bt + static_cast<long long>(b) * P.max_blocks[w] + lp)
+                          : b * P.max_blocks[w] + lp;
       if (pg < 0 || pg >= P.num_pages[w]) {
         raise_err(P.d_err, DSA_DEVERR_PAGE);
         return;
@@ -581,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
 
 template <int H, bool F>
 cudaError_t launch_one(const MlaLaunch& p, cudaStream_t stream, bool pdl) {
-  const MlaSmem S = mla_smem(H, F, p.chunk);
+  const MlaSmem S = mla_smem(H, F, p.chunk, p.bt_smem);
   cudaError_t e = cudaFuncSetAttribute(sparse_mla_kernel<H, F>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, S.total);
   if (e != cudaSuccess) return e;
@@ -606,8 +624,19 @@ int auto_mla_splits(int work_rows, int k, int expected_count) {
   return s;
 }
 
-cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream, bool pdl) {
-  if (p.nshards * p.rows == 0 || p.num_splits == 0) return cudaSuccess;
+cudaError_t launch_sparse_mla(const MlaLaunch& p0, cudaStream_t stream, bool pdl) {
+  if (p0.nshards * p0.rows == 0 || p0.num_splits == 0) return cudaSuccess;
+  // keep a request's block-table row in shared memory when it is short
+  // enough and fits beside the tiles
+  MlaLaunch p = p0;
+  int maxb = 0;
+  for (int i = 0; i < p.nshards; ++i)
+    if (p.block_table[i] != nullptr && p.max_blocks[i] > maxb) maxb = p.max_blocks[i];
+  constexpr int kBtSmemCap = 4096;
+  p.bt_smem = (maxb > 0 && maxb <= kBtSmemCap &&
+               mla_smem(p.heads, p.fp8, p.chunk, maxb).total <= 227 * 1024)
+                  ? maxb
+                  : 0;
   if (p.heads == 16)
     return p.fp8 ? launch_one<16, true>(p, stream, pdl) : launch_one<16, false>(p, stream, pdl);
   if (p.heads == 32)
