@@ -354,31 +354,52 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
 
     if (warp == 0) {
       // ------------------------------------------------ TMA producer
-      if (lane == 0) {
-        Walker wk;
-        wk.start(P, rm, start_pair, start_tile);
-        int stage = 0;
-        uint32_t phase = 0;
-        int issued = 0;
-        for (int u = 0; u < nunits; ++u) {
-          if (!mbar_wait(bar(B_KEMPTY + stage), phase ^ 1u, abort_flag)) break;
-          ++issued;
-          const int sl = pair_shard(P, wk.pair);
-          const int b = pair_req(P, wk.pair);
-          int pages[2] = {-1, -1}, slots[2] = {0, 0};
-          uint32_t bytes = 0;
-          for (int h = 0; h < 2; ++h) {
-            const int t0 = wk.tile * kTileT + h * 64;
-            if (t0 >= wk.pi.len) break;
-            const int pg = page_of(P, sl, b, t0 / P.page_size);
-            if (pg < 0 || pg >= P.num_pages[sl]) {
-              raise_err(P.d_err, DSA_DEVERR_PAGE);
-              continue;
-            }
-            pages[h] = pg;
-            slots[h] = t0 % P.page_size;
-            bytes += kFp8 ? 64u * 128u : 2u * kHalfBf16Box;
+      // The whole warp walks the units and lane 0 issues the copies.  The
+      // block-table entries are read 32 at a time (one coalesced load holds
+      // the pages of 16 tiles) and handed to lane 0 by a shuffle, so that a
+      // tile waits for no global load of its own.
+      Walker wk;
+      wk.start(P, rm, start_pair, start_tile);
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      int pc_pair = -1, pc_base = 0, pc_val = -1;  // this lane holds entry pc_base + lane
+      for (int u = 0; u < nunits; ++u) {
+        const bool got = __shfl_sync(
+            0xffffffffu,
+            lane == 0 ? mbar_wait(bar(B_KEMPTY + stage), phase ^ 1u, abort_flag) : true, 0);
+        if (!got) break;
+        ++issued;
+        const int sl = pair_shard(P, wk.pair);
+        const int b = pair_req(P, wk.pair);
+        const int32_t* bt = P.block_table[sl];
+        const int t0 = wk.tile * kTileT;
+        const int lpa = t0 / P.page_size;  // the tile's first page
+        if (bt != nullptr && (wk.pair != pc_pair || lpa < pc_base || lpa + 1 >= pc_base + 32)) {
+          pc_pair = wk.pair;
+          pc_base = lpa;
+          const int e = pc_base + lane;
+          pc_val = e < P.max_blocks[sl]
+                       ? __ldg(bt + static_cast<long long>(b) * P.max_blocks[sl] + e)
+                       : -1;
+        }
+        int pages[2] = {-1, -1}, slots[2] = {0, 0};
+        uint32_t bytes = 0;
+        for (int h = 0; h < 2; ++h) {
+          const int th = t0 + h * 64;
+          const int lp = th / P.page_size;
+          const int cached = __shfl_sync(0xffffffffu, pc_val, (lp - pc_base) & 31);
+          if (th >= wk.pi.len) continue;
+          const int pg = bt != nullptr ? cached : b * P.max_blocks[sl] + lp;
+          if (pg < 0 || pg >= P.num_pages[sl]) {
+            if (lane == 0) raise_err(P.d_err, DSA_DEVERR_PAGE);
+            continue;
           }
+          pages[h] = pg;
+          slots[h] = th % P.page_size;
+          bytes += kFp8 ? 64u * 128u : 2u * kHalfBf16Box;
+        }
+        if (lane == 0) {
           const uint32_t fb = bar(B_KFULL + stage);
           const uint32_t dst = ring + stage * L.stage_bytes;
           if (kFp8) {
@@ -401,12 +422,14 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
               tma_load_3d(dst + 16384 + h * 8192, &P.kmap[sl], fb, 64, slots[h], pages[h]);
             }
           }
-          if (++stage == L.stages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          wk.next(P);
         }
+        if (++stage == L.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        wk.next(P);
+      }
+      if (lane == 0) {
         // every stage's last release before the CTA exits (the epilogue is
         // behind this thread), so that no barrier is left mid-phase
         if (!*abort_flag) {
