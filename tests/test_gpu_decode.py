@@ -72,6 +72,46 @@ def test_more_rows_than_declared_sets_error_bit():
     assert run.run() & C.DSA_DEVERR_GROUP
 
 
+@pytest.mark.parametrize("k", [1, 100, 1000, 4096])
+def test_decode_other_k(k):
+    """k other than 2048: a single token, fewer than a tile, not a multiple
+    of 64, and the largest k the entry points accept."""
+    _run(config_spec(1, B=2, L=5000, topk=k))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_cache_write_then_decode(dtype):
+    """One decode step's cache write feeds the decode: new rows (RoPE'd, and
+    quantized for fp8 caches) go to each request's last 5 positions through
+    the block tables; the decode at the last position then matches the oracle
+    run on the caches as written."""
+    from dsa_sparse_attention_decode_gb300 import api
+    from workloads.device import upload as _upload
+    from workloads.synth import to_bf16_bits
+    wl = make_workload(config_spec(1, B=2, L=4000, dtype=dtype))
+    dw = _upload(wl, "cuda")
+    rng = np.random.default_rng(21)
+    n_new = 5
+    req = np.repeat(np.arange(wl.B, dtype=np.int32), n_new)
+    pos = np.concatenate([np.arange(int(wl.row_pos[b]) - n_new + 1, int(wl.row_pos[b]) + 1)
+                          for b in range(wl.B)]).astype(np.int32)
+    kv_in = to_bf16_bits(rng.standard_normal((len(pos), 576)) * 0.5)
+    ix_in = to_bf16_bits(rng.standard_normal((len(pos), 128)))
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.dsa_cache_write(t(kv_in.view(np.int16)), t(req), t(pos), wl.B, [dw.kv], err,
+                        idx_in=t(ix_in.view(np.int16)), idx_k=[dw.idx_k])
+    assert api.dsa_read_error(err) == 0
+    # the oracle reads the caches exactly as the kernel wrote them
+    for host, dev in ((wl.kv, dw.kv), (wl.idx_k, dw.idx_k)):
+        host.data[...] = dev.data.cpu().numpy().view(host.data.dtype)
+        if host.scale is not None:
+            host.scale[...] = dev.scale.cpu().numpy()
+    run = DecodeRun(dw)
+    assert run.run() == 0
+    check_decode_rows(run, range(wl.R))
+
+
 @pytest.mark.parametrize("S", [1, 2, 7, 32])
 def test_split_counts_agree(S):
     _run(config_spec(1, B=2, L=4500), num_splits=S)
