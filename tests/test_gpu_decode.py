@@ -112,6 +112,31 @@ def test_cache_write_then_decode(dtype):
     check_decode_rows(run, range(wl.R))
 
 
+def test_many_rows_read_metadata_from_global():
+    """2400 query rows: the row metadata no longer fits the indexer's shared-
+    memory copy, and the schedule reads it from global memory instead."""
+    wl, run, _ = _run(config_spec(2, B=400, L_lo=300, L_hi=700, rows_per_req=6),
+                      rows=range(0, 2400, 97))
+    assert wl.R == 2400
+
+
+def test_wide_block_table_reads_global():
+    """A block table wider than the MLA's shared-memory copy (4096 entries per
+    request): the gather reads the global table."""
+    import dataclasses
+    wl = make_workload(config_spec(1, B=2, L=3000))
+    dw = upload(wl, "cuda")
+    wide = 5000
+    for name in ("kv", "idx_k"):
+        c = getattr(dw, name)
+        bt = torch.full((c.block_table.shape[0], wide), -1, dtype=torch.int32, device="cuda")
+        bt[:, : c.block_table.shape[1]] = c.block_table
+        setattr(dw, name, dataclasses.replace(c, block_table=bt, max_blocks=wide))
+    run = DecodeRun(dw)
+    assert run.run() == 0
+    check_decode_rows(run, range(wl.R))
+
+
 @pytest.mark.parametrize("S", [1, 2, 7, 32])
 def test_split_counts_agree(S):
     _run(config_spec(1, B=2, L=4500), num_splits=S)
