@@ -47,18 +47,18 @@ constexpr int kWdef = 128;     // [32] per warp: keys above the bin b1
 constexpr int kPub = 160;      // [16] read by the cluster: min, max, candidates, keys above b1
 constexpr int kTmp = 192;      // [64] reductions
 constexpr int kCtaCnt = 256;   // [8] per CTA of the cluster: keys above T, keys equal to T
+constexpr int kWtot = 320;     // [32] per warp: the bin search's suffix sums
 constexpr int kMiscWords = 512;
 
 struct TopkSmem {
   int cap;         // keys of the CTA's segment cached in smem
-  int off_hist, off_red, off_misc, off_cand, off_all, off_keys, total;
+  int off_hist, off_misc, off_cand, off_all, off_keys, total;
 };
 
 __host__ inline TopkSmem topk_smem(int C) {
   TopkSmem s{};
   s.off_hist = 0;                                  // this CTA's histogram (read by the cluster)
-  s.off_red = s.off_hist + kBins * 4;              // the cluster's summed histogram
-  s.off_misc = s.off_red + (C > 1 ? kBins * 4 : 0);
+  s.off_misc = s.off_hist + kBins * 4;
   s.off_cand = s.off_misc + kMiscWords * 4;        // this CTA's candidates (key, position)
   s.off_all = s.off_cand + kCand * 8;              // the cluster's candidates
   s.off_keys = s.off_all + (C > 1 ? kCand * 8 : 0);
@@ -75,25 +75,6 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, int lane) {
     if (lane >= o) v += t;
   }
   return v;
-}
-
-// red[b] = sum over the cluster's CTAs of hist[b], b < nb (nb a multiple of 4)
-template <int C>
-__device__ __forceinline__ void cluster_sum_hist(const uint32_t* hist, uint32_t* red, int nb) {
-  const uint32_t base = smem_u32(hist);
-  for (int v = threadIdx.x; v < nb / 4; v += kThreads) {
-    uint4 acc = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int c = 0; c < C; ++c) {
-      const uint4 x = dsmem_ld_v4(dsmem_map(base + v * 16, c));
-      acc.x += x.x;
-      acc.y += x.y;
-      acc.z += x.z;
-      acc.w += x.w;
-    }
-    reinterpret_cast<uint4*>(red)[v] = acc;
-  }
-  __syncthreads();
 }
 
 // sum of v over the lanes at and above this one
@@ -158,12 +139,79 @@ __device__ void warp_find_bin(const uint32_t* hist, int nb, uint32_t k_rem, uint
   __syncwarp();
 }
 
+__device__ __forceinline__ uint2 dsmem_ld_v2(uint32_t caddr) {
+  uint2 v;
+  asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(caddr)
+               : "memory");
+  return v;
+}
+
+// Every thread of the CTA: the bin of the cluster's histogram (the sum over
+// the cluster's CTAs of hist[0, nb), nb a power of two up to kBins; a higher
+// bin holds larger keys) that holds the k_rem-th largest key.  For C > 1 the
+// caller has passed a cluster barrier after every CTA's histogram, and no CTA
+// writes its histogram again before the next one.  Thread t sums its own
+// nb / kThreads bins (at least one; threads past nb hold none) over the
+// cluster, a suffix sum over the threads (per warp, then over the 32 warp
+// totals in wtot) gives the keys above them, and the one thread whose bins
+// hold the k_rem-th key writes (bin, k_rem within the bin, the bin's count)
+// to out[0..2].  The caller's __syncthreads publishes them.
+template <int C>
+__device__ __forceinline__ void cta_find_bin(const uint32_t* hist, int nb, uint32_t k_rem,
+                                             uint32_t* out, uint32_t* wtot, int tid) {
+  static_assert(kWarps == 32 && kThreads * 2 >= kBins, "one warp total per lane, two bins per thread");
+  const int lane = tid & 31, warp = tid >> 5;
+  const bool two = nb > kThreads;  // two bins per thread
+  const int b0 = two ? 2 * tid : tid;
+  uint32_t h0 = 0, h1 = 0;
+  if (b0 < nb) {
+    if constexpr (C > 1) {
+      const uint32_t a = smem_u32(hist + b0);
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        if (two) {
+          const uint2 x = dsmem_ld_v2(dsmem_map(a, c));
+          h0 += x.x;
+          h1 += x.y;
+        } else {
+          h0 += dsmem_ld(dsmem_map(a, c));
+        }
+      }
+    } else if (two) {
+      const uint2 x = *reinterpret_cast<const uint2*>(hist + b0);
+      h0 = x.x;
+      h1 = x.y;
+    } else {
+      h0 = hist[b0];
+    }
+  }
+  const uint32_t mine = h0 + h1;
+  const uint32_t incl = warp_suffix_incl(mine, lane);
+  if (lane == 0) wtot[warp] = incl;
+  __syncthreads();
+  const uint32_t wt = wtot[lane];
+  const uint32_t wincl = warp_suffix_incl(wt, lane);
+  const uint32_t total = __shfl_sync(0xffffffffu, wincl, 0);
+  const uint32_t above = __shfl_sync(0xffffffffu, wincl - wt, warp) + (incl - mine);
+  // thread 0 answers (with its lowest bin) if the histogram holds fewer keys
+  if ((above < k_rem && above + mine >= k_rem) || (tid == 0 && total < k_rem)) {
+    if (two && above + h1 >= k_rem) {
+      out[0] = static_cast<uint32_t>(b0 + 1);
+      out[1] = k_rem - above;
+      out[2] = h1;
+    } else {
+      out[0] = static_cast<uint32_t>(b0);
+      out[1] = k_rem - (above + h1);
+      out[2] = h0;
+    }
+  }
+}
+
 template <int C>
 __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
     topk_kernel(const TopkLaunch P, const TopkSmem S) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + S.off_hist);
-  uint32_t* red = C > 1 ? reinterpret_cast<uint32_t*>(smem + S.off_red) : hist;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + S.off_misc);
   uint2* cand = reinterpret_cast<uint2*>(smem + S.off_cand);
   uint2* cand_all = C > 1 ? reinterpret_cast<uint2*>(smem + S.off_all) : cand;
@@ -173,6 +221,7 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
   uint32_t* weq = misc + kWeq;
   uint32_t* wdef = misc + kWdef;
   uint32_t* pub = misc + kPub;
+  uint32_t* wtot = misc + kWtot;
   uint32_t* tmp = misc + kTmp;
   uint32_t* ctacnt = misc + kCtaCnt;
 
@@ -342,8 +391,7 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
       const int nbits = min(kRoundBits, top + 1);
       lo = top + 1 - nbits;
       const int nb = 1 << nbits;
-      const int nbz = max(nb, 4);
-      for (int b = tid; b < nbz; b += kThreads) hist[b] = 0;
+      for (int b = tid; b < nb; b += kThreads) hist[b] = 0;
       __syncthreads();
       const uint32_t bmask = static_cast<uint32_t>(nb - 1);
       for (int j4 = tid; j4 < (cached >> 2); j4 += kThreads) {
@@ -356,11 +404,8 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
       for (int j = (cached & ~3) + tid; j < m; j += kThreads)
         atomicAdd(hist + ((key_at(j) >> lo) & bmask), 1u);
       __syncthreads();
-      if constexpr (C > 1) {
-        cluster_sync();  // every CTA's histogram is complete
-        cluster_sum_hist<C>(hist, red, nbz);
-      }
-      if (warp == 0) warp_find_bin(red, nb, static_cast<uint32_t>(k), sh + 4, lane);
+      if constexpr (C > 1) cluster_sync();  // every CTA's histogram is complete
+      cta_find_bin<C>(hist, nb, static_cast<uint32_t>(k), sh + 4, wtot, tid);
       __syncthreads();
       pre = ((static_cast<uint64_t>(kmax) >> (top + 1)) << nbits) | sh[4];
       k_rem = sh[5];
@@ -524,8 +569,7 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
       const int nbits = min(kRoundBits, t + 1);
       const int lo2 = t + 1 - nbits;
       const int nb = 1 << nbits;
-      const int nbz = max(nb, 4);
-      for (int b = tid; b < nbz; b += kThreads) hist[b] = 0;
+      for (int b = tid; b < nb; b += kThreads) hist[b] = 0;
       __syncthreads();
       for (int j = tid; j < m; j += kThreads) {
         const uint32_t key = key_at(j);
@@ -533,11 +577,8 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
           atomicAdd(hist + ((key >> lo2) & static_cast<uint32_t>(nb - 1)), 1u);
       }
       __syncthreads();
-      if constexpr (C > 1) {
-        cluster_sync();
-        cluster_sum_hist<C>(hist, red, nbz);
-      }
-      if (warp == 0) warp_find_bin(red, nb, k_rem, sh + 4, lane);
+      if constexpr (C > 1) cluster_sync();
+      cta_find_bin<C>(hist, nb, k_rem, sh + 4, wtot, tid);
       __syncthreads();
       pre = (pre << nbits) | sh[4];
       k_rem = sh[5];
