@@ -7,15 +7,18 @@
 // with a single split the partial is the final result and goes straight to
 // the caller's output.
 //
-// One CTA per (work row, split), 10 warps.  The split's selected positions are
-// resolved through the block table once.  Warps 8-9 then gather 64-token tiles
-// of 576-wide latent rows with 16-byte cp.async into a double buffer (each
-// thread's copies arrive on the tile's mbarrier as they land), so the gather
-// runs while warps 0-7 compute on the previous tile; fp8 rows land raw and are
-// widened to f16 by the compute warps (e4m3 values are f16 values).  Every head
-// of the row shares each gathered tile:
+// One CTA per (work row, split), 10 warps.  Warps 8-9 gather 64-token tiles
+// of 576-wide latent rows into a double buffer, one bulk copy per selected row
+// (selection -> block table -> row, resolved one tile ahead), each landing on
+// the tile's mbarrier, so the gather runs while warps 0-7 compute on the
+// previous tile; fp8 rows land raw and are widened to f16 by the compute warps
+// (e4m3 values are f16 values).  Every head of the row shares each gathered
+// tile:
 //   S = q . kv^T (all 576 dims), online softmax in fp32 (base 2), P split into
 //   two bf16 parts (f16 for fp8 rows), O += P . v (first 512 dims).
+// With bf16 rows and 32 heads the compute warps form two groups of 16 heads
+// that take turns on S, so that one group's S (shared-memory reads) overlaps
+// the other's P . v (tensor pipe).
 // The fp8 path multiplies each logit by the token's scale and folds the scale
 // into P for the value product; its query is converted to f16 with a per-head
 // power-of-two factor that the logit scale undoes.
@@ -89,6 +92,11 @@ DSA_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, 
                : "r"(addr));
 }
 
+// arrive on named barrier `id` (of `nthreads` threads) without waiting
+DSA_DEV void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 template <bool kF16>
 DSA_DEV void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                       uint32_t b1) {
@@ -121,9 +129,17 @@ DSA_DEV uint32_t pack2(float lo, float hi) {
 // H heads (16 or 32); kFp8: e4m3 cache, f16 MMAs; else bf16 cache and MMAs.
 template <int H, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch P) {
-  constexpr int MT = H / 16;             // m16 tiles of heads
-  constexpr int NTW = MT;                // n8 token tiles per warp in S = q.kv^T
-  constexpr int TGS = 8 / MT;            // token groups
+  // The compute warps form kGroups groups, each owning H / kGroups heads with
+  // its own online softmax and O.  Two groups (bf16, 32 heads) take turns on
+  // S = q.kv^T, which is bound by shared-memory reads, so that one group's S
+  // runs while the other's O += P.v keeps the tensor pipe busy.  The fp8 path
+  // (one widened tile buffer) and 16 heads (one m16 tile) use one group.
+  constexpr int kGroups = (!kFp8 && H == 32) ? 2 : 1;
+  constexpr int kGW = (kCompute / 32) / kGroups;  // warps per group
+  constexpr int MT = H / kGroups / 16;   // m16 tiles of the group's heads
+  constexpr int TGS = kGW / MT;          // token groups of S
+  constexpr int NTW = 8 / TGS;           // n8 token tiles per warp in S
+  constexpr int DW = kVDim / kGW;        // value dims per warp in O += P.v
   extern __shared__ __align__(16) uint8_t smem[];
   const MlaSmem S = mla_smem(H, kFp8, P.chunk, P.bt_smem);
   uint8_t* q_s = smem + S.off_q;
@@ -170,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(bars + i), kGather);   // tile landed: every gather thread's copies
-      mbar_init(smem_u32(bars + 2 + i), 1);     // buffer free: one compute thread
+      mbar_init(smem_u32(bars + 2 + i), kGroups);  // buffer free: one thread per group
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -325,12 +341,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
       }
     }
     named_bar_sync(1, kCompute);  // the query is in shared memory
-    // per-thread state: O accumulators for dims [64*warp, 64*warp+64) of all heads
-    float o[MT][8][4];
+    const int grp = warp / kGW, wg = warp - grp * kGW;  // group, warp within it
+    const int mt0 = grp * MT;                           // the group's first head tile
+    // the group's barrier (id 1 when a single group spans all compute warps)
+    const int gbar = kGroups == 1 ? 1 : 2 + grp;
+    // per-thread state: O accumulators for dims [DW*wg, DW*wg+DW) of the group's heads
+    float o[MT][DW / 8][4];
 #pragma unroll
     for (int a = 0; a < MT; ++a)
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < DW / 8; ++j)
 #pragma unroll
         for (int c = 0; c < 4; ++c) o[a][j][c] = 0.0f;
     float m_run[MT][2];
@@ -338,11 +358,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
     for (int a = 0; a < MT; ++a) m_run[a][0] = m_run[a][1] = -__int_as_float(0x7f800000);
     float l_part[2] = {0.0f, 0.0f};  // row sums of this thread's S rows
 
-    const int mt_s = warp % MT;          // S role: head tile
-    const int tg = warp / MT;            // S role: token group
+    const int ml_s = wg % MT;            // S role: head tile within the group
+    const int mt_s = mt0 + ml_s;         // S role: head tile
+    const int tg = wg / MT;              // S role: token group
     const int n_s0 = tg * (8 * NTW);     // first token of the group in the tile
     const float qsc0 = qexp[mt_s * 16 + g];
     const float qsc1 = qexp[mt_s * 16 + g + 8];
+    // S turns: group 0 computes S of tile i once group 1 is done with S of
+    // tile i - 1 (barrier 4), group 1 once group 0 is done with S of tile i
+    // (barrier 5); group 1's first arrival opens group 0's first turn
+    if (kGroups == 2 && grp == 1) named_bar_arrive(4, kCompute);
 
     for (int tile = 0; tile < ntiles; ++tile) {
       const int fb = tile & 1;  // the gathered tile's buffer (raw rows for fp8)
@@ -374,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
       const int t0 = tile * kTile;
       const uint32_t kv_a = smem_u32(kv);
       const uint32_t q_a = smem_u32(q_s);
+      if (kGroups == 2) named_bar_sync(4 + grp, kCompute);  // this group's S turn
 
       // ---- S = q . kv^T for head tile mt_s, tokens n_s0 .. n_s0 + 8*NTW
       // Software-pipelined: the fragments of step kk + 1 are requested before
@@ -415,6 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
 #pragma unroll
           for (int c = 0; c < 4; ++c) sacc[j][c] = sacc2[0][j][c] + sacc2[1][j][c];
       }
+      // the other group's S turn (group 1 opens no turn after its last tile)
+      if (kGroups == 2 && !(grp == 1 && tile + 1 == ntiles)) named_bar_arrive(5 - grp, kCompute);
       // logits in base 2, masked past the split's end
       float mx0 = -__int_as_float(0x7f800000), mx1 = mx0;
 #pragma unroll
@@ -441,14 +469,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
         red[tg * H + mt_s * 16 + g] = mx0;
         red[tg * H + mt_s * 16 + g + 8] = mx1;
       }
-      named_bar_sync(1, kCompute);
+      named_bar_sync(gbar, kGW * 32);
       // new running max for every head row this thread touches
       float alpha[MT][2];
 #pragma unroll
       for (int a = 0; a < MT; ++a) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int h = a * 16 + g + hh * 8;
+          const int h = (mt0 + a) * 16 + g + hh * 8;
           float tm = red[h];
 #pragma unroll
           for (int x = 1; x < TGS; ++x) tm = fmaxf(tm, red[x * H + h]);
@@ -460,8 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
       }
       // P for the S rows of this warp
       {
-        const float mA = (m_run[mt_s][0] == -__int_as_float(0x7f800000)) ? 0.0f : m_run[mt_s][0];
-        const float mB = (m_run[mt_s][1] == -__int_as_float(0x7f800000)) ? 0.0f : m_run[mt_s][1];
+        const float mA = (m_run[ml_s][0] == -__int_as_float(0x7f800000)) ? 0.0f : m_run[ml_s][0];
+        const float mB = (m_run[ml_s][1] == -__int_as_float(0x7f800000)) ? 0.0f : m_run[ml_s][1];
         float ls0 = 0.0f, ls1 = 0.0f;
 #pragma unroll
         for (int j = 0; j < NTW; ++j) {
@@ -491,28 +519,29 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
                 pack2<false>(v10 - __uint_as_float(h1 << 16), v11 - __uint_as_float(h1 & 0xFFFF0000u));
           }
         }
-        l_part[0] = l_part[0] * alpha[mt_s][0] + ls0;
-        l_part[1] = l_part[1] * alpha[mt_s][1] + ls1;
+        l_part[0] = l_part[0] * alpha[ml_s][0] + ls0;
+        l_part[1] = l_part[1] * alpha[ml_s][1] + ls1;
       }
-      named_bar_sync(1, kCompute);
+      named_bar_sync(gbar, kGW * 32);
 
-      // ---- O += P . v for value dims [64*warp, 64*warp + 64)
+      // ---- O += P . v for value dims [DW*wg, DW*wg + DW) of the group's heads
 #pragma unroll
       for (int a = 0; a < MT; ++a)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < DW / 8; ++j) {
           o[a][j][0] *= alpha[a][0];
           o[a][j][1] *= alpha[a][0];
           o[a][j][2] *= alpha[a][1];
           o[a][j][3] *= alpha[a][1];
         }
       {
-        // 16 steps (4 token slices x 4 pairs of 8-dim column tiles), each
-        // step's fragments requested one step ahead; the hi terms of P issue
-        // before the lo terms so that no MMA waits for its accumulator
-        const uint32_t p_a = smem_u32(p_s) + (lane & 15) * kPRowB + (lane >> 4) * 16;
+        // 4 token slices x DW / 16 pairs of 8-dim column tiles, each step's
+        // fragments requested one step ahead; the hi terms of P issue before
+        // the lo terms so that no MMA waits for its accumulator
+        constexpr int kJP = DW / 16;  // column-tile pairs per token slice
+        const uint32_t p_a = smem_u32(p_s) + (mt0 * 16 + (lane & 15)) * kPRowB + (lane >> 4) * 16;
         const uint32_t v_a =
-            kv_a + ((lane & 7) + ((lane >> 3) & 1) * 8) * kRowB + (warp * 64 + (lane >> 4) * 8) * 2;
+            kv_a + ((lane & 7) + ((lane >> 3) & 1) * 8) * kRowB + (wg * DW + (lane >> 4) * 8) * 2;
         uint32_t af[2][MT][4], al[2][MT][4], bv[2][4];
         auto load_p = [&](int kk, int sl) {
 #pragma unroll
@@ -525,16 +554,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
           }
         };
         auto load_v = [&](int st, int sl) {
-          const int kk = st >> 2, jp = st & 3;
+          const int kk = st / kJP, jp = st % kJP;
           ldsm_x4_t(v_a + kk * 16 * kRowB + jp * 32, bv[sl][0], bv[sl][1], bv[sl][2], bv[sl][3]);
         };
         load_p(0, 0);
         load_v(0, 0);
 #pragma unroll
-        for (int st = 0; st < (kTile / 16) * 4; ++st) {
-          const int kk = st >> 2, j = (st & 3) * 2, sv = st & 1, sp = kk & 1;
-          if (st + 1 < (kTile / 16) * 4) {
-            if (((st + 1) & 3) == 0) load_p(kk + 1, sp ^ 1);
+        for (int st = 0; st < (kTile / 16) * kJP; ++st) {
+          const int kk = st / kJP, j = (st % kJP) * 2, sv = st & 1, sp = kk & 1;
+          if (st + 1 < (kTile / 16) * kJP) {
+            if ((st + 1) % kJP == 0) load_p(kk + 1, sp ^ 1);
             load_v(st + 1, sv ^ 1);
           }
 #pragma unroll
@@ -555,8 +584,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
           }
         }
       }
-      named_bar_sync(1, kCompute);
-      if (!kFp8 && tid == 0) mbar_arrive(smem_u32(bars + 2 + fb));  // the tile's buffer is free
+      named_bar_sync(gbar, kGW * 32);
+      // the tile's buffer is free once every group is past it
+      if (!kFp8 && wg == 0 && lane == 0) mbar_arrive(smem_u32(bars + 2 + fb));
     }
 
     // ---- softmax denominators: sum the row partials over t4 and token groups
@@ -570,23 +600,23 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
       red2[tg * H + mt_s * 16 + g] = l0;
       red2[tg * H + mt_s * 16 + g + 8] = l1;
     }
-    named_bar_sync(1, kCompute);
-    const int d0 = warp * 64;
+    named_bar_sync(gbar, kGW * 32);
+    const int d0 = wg * DW;
 #pragma unroll
     for (int a = 0; a < MT; ++a) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int h = a * 16 + g + hh * 8;
+        const int h = (mt0 + a) * 16 + g + hh * 8;
         float l = 0.0f;
 #pragma unroll
         for (int x = 0; x < TGS; ++x) l += red2[x * H + h];
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < DW / 8; ++j) {
           float2 v = make_float2(o[a][j][2 * hh] * inv, o[a][j][2 * hh + 1] * inv);
           *reinterpret_cast<float2*>(out_o + h * kVDim + d0 + 8 * j + 2 * t4) = v;
         }
-        if (warp == 0 && t4 == 0) {
+        if (wg == 0 && t4 == 0) {
           out_l[h] = l > 0.0f ? (m_run[a][hh] + log2f(l)) * kLn2 : -__int_as_float(0x7f800000);
         }
       }
