@@ -228,6 +228,7 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;  // the lanes below this one
   const uint32_t crank = C > 1 ? cluster_ctarank() : 0u;
   const int q = blockIdx.x / C;
   const int w = q / P.rows;
@@ -421,20 +422,20 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t kv[4];
       bool ok[4];
       load4(j0, s1, kv, ok);
-      uint32_t nc = 0;
+      uint32_t c_lo = 0, tot = 0;  // candidates in lower lanes / in the warp
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const uint64_t hi = kv[e] >> lo;
         ndef += (ok[e] && hi > pre) ? 1u : 0u;
-        nc += (ok[e] && hi == pre) ? 1u : 0u;
+        const uint32_t b = __ballot_sync(0xffffffffu, ok[e] && hi == pre);
+        c_lo += __popc(b & lt_mask);
+        tot += __popc(b);
       }
-      const uint32_t incl = warp_incl_scan(nc, lane);
-      const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
       if (tot != 0) {
         uint32_t base = 0;
-        if (lane == 31) base = atomicAdd(sh + 8, tot);
-        base = __shfl_sync(0xffffffffu, base, 31);
-        uint32_t slot = base + incl - nc;
+        if (lane == 0) base = atomicAdd(sh + 8, tot);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        uint32_t slot = base + c_lo;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           if (ok[e] && (static_cast<uint64_t>(kv[e] >> lo) == pre)) {
@@ -672,17 +673,21 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
       load4(j0, s1, kv, ok);
     }
+    // position order is lane-major (lane l holds positions j0 .. j0 + 3), so
+    // the ties and selections before this lane's first are the lower lanes'
+    // bits of one ballot per e
     bool eqf[4];
-    uint32_t neq = 0;
+    uint32_t eq_lo = 0, eq_all = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       eqf[e] = ok[e] && !all && kv[e] == T;
-      neq += eqf[e] ? 1u : 0u;
+      const uint32_t b = __ballot_sync(0xffffffffu, eqf[e]);
+      eq_lo += __popc(b & lt_mask);
+      eq_all += __popc(b);
     }
-    const uint32_t eincl = warp_incl_scan(neq, lane);
-    uint32_t er = eq_before + eincl - neq;  // rank of this lane's first tie
+    uint32_t er = eq_before + eq_lo;  // rank of this lane's first tie
     bool self[4];
-    uint32_t nsel = 0;
+    uint32_t sel_lo = 0, sel_all = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       if (eqf[e]) {
@@ -691,10 +696,11 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
       } else {
         self[e] = ok[e] && (all || kv[e] > T);
       }
-      nsel += self[e] ? 1u : 0u;
+      const uint32_t b = __ballot_sync(0xffffffffu, self[e]);
+      sel_lo += __popc(b & lt_mask);
+      sel_all += __popc(b);
     }
-    const uint32_t sincl = warp_incl_scan(nsel, lane);
-    uint32_t slot = sel_before + sincl - nsel;  // selections before this lane's first
+    uint32_t slot = sel_before + sel_lo;  // selections before this lane's first
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       if (self[e]) {
@@ -704,8 +710,8 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
         ++slot;
       }
     }
-    eq_before += __shfl_sync(0xffffffffu, eincl, 31);
-    sel_before += __shfl_sync(0xffffffffu, sincl, 31);
+    eq_before += eq_all;
+    sel_before += sel_all;
   }
   if (crank == 0) {
     for (int i = cnt_all + tid; i < k; i += kThreads) {
