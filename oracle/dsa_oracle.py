@@ -170,6 +170,21 @@ def mla_attention(q: np.ndarray, KV: np.ndarray, tau: float, dv: int = 512
     return p @ KV[:, :dv], lse
 
 
+def mla_attention_into(q: np.ndarray, KV: np.ndarray, tau: float, dv: int = 512
+                       ) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """The three outputs of a sparse-prefill call that writes into caller-owned
+    buffers (DSpark page, section 6.3: output, max-logit and LSE together):
+    O and lse as in mla_attention, and max_logit = max over the selected rows
+    of z = tau * q . kv (natural units, the scaled logit itself), -inf when
+    nothing is selected.  lse - ln(m) <= max_logit <= lse for m rows."""
+    O, lse = mla_attention(q, KV, tau, dv)
+    H = np.asarray(q).shape[0]
+    if np.asarray(KV).shape[0] == 0:
+        return O, np.full(H, NEG_INF), lse
+    z = tau * (np.asarray(q, dtype=np.float64) @ np.asarray(KV, dtype=np.float64).T)
+    return O, z.max(axis=1), lse
+
+
 def lse_merge(O_parts: np.ndarray, lse_parts: np.ndarray
               ) -> Tuple[np.ndarray, np.ndarray]:
     """Merge partial attention results that each cover a disjoint part of the
@@ -246,6 +261,15 @@ def row_attention(wl, r: int, positions: np.ndarray, cache=None):
     KV = cache_rows(cache, b, positions)
     q = bf16_bits_to_f64(wl.q[r])
     return mla_attention(q, KV, wl.sm_scale)
+
+
+def row_attention_into(wl, r: int, positions: np.ndarray, cache=None):
+    """mla_attention_into for query row r of workload wl."""
+    b = int(wl.row_req[r])
+    cache = wl.kv if cache is None else cache
+    KV = cache_rows(cache, b, positions)
+    q = bf16_bits_to_f64(wl.q[r])
+    return mla_attention_into(q, KV, wl.sm_scale)
 
 
 def decode_row(wl, r: int, scores: Optional[np.ndarray] = None):

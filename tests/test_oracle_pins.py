@@ -217,6 +217,49 @@ def test_attention_equals_masked_dense_softmax():
     assert np.allclose(O, p @ KV[:, :512], rtol=1e-12, atol=1e-14)
 
 
+def test_attention_into_hand_worked():
+    g = json.load(open(os.path.join(GOLD, "hand_worked_decode.json")))["attention"]
+    KV = np.array([[_expr(x) for x in row] for row in g["KV"]])
+    O, mx, lse = orc.mla_attention_into(np.array(g["q"], float), KV, g["tau"], dv=g["dv"])
+    assert np.allclose(mx, [_expr(x) for x in g["max_logit"]], rtol=1e-14)
+    assert np.allclose(O, [[_expr(x) for x in r] for r in g["O"]], rtol=1e-14)
+    assert np.allclose(lse, [_expr(x) for x in g["lse"]], rtol=1e-14)
+
+
+def test_attention_into_max_logit_brute_force_and_bounds():
+    rng = random.Random(11)
+    H, D, m, tau = 3, 5, 7, 0.6
+    q = [[rng.uniform(-2, 2) for _ in range(D)] for _ in range(H)]
+    KV = [[rng.uniform(-2, 2) for _ in range(D)] for _ in range(m)]
+    _, mx, lse = orc.mla_attention_into(np.array(q), np.array(KV), tau, dv=2)
+    for h in range(H):
+        z = [tau * sum(q[h][i] * KV[t][i] for i in range(D)) for t in range(m)]
+        assert abs(mx[h] - max(z)) < 1e-13
+        # lse - ln m <= max <= lse
+        assert lse[h] - math.log(m) - 1e-13 <= mx[h] <= lse[h] + 1e-13
+
+
+def test_attention_into_closed_forms():
+    rng = np.random.default_rng(12)
+    tau = 576 ** -0.5
+    q = rng.standard_normal((16, 576)) * 0.5
+    kv = rng.standard_normal((1, 576)) * 0.5
+    # one row: max logit = lse = z
+    _, mx, lse = orc.mla_attention_into(q, kv, tau)
+    assert np.allclose(mx, tau * (q @ kv[0])) and np.allclose(mx, lse)
+    # identical rows: the max is z, the lse z + ln m
+    _, mx2, lse2 = orc.mla_attention_into(q, np.repeat(kv, 5, axis=0), tau)
+    assert np.allclose(mx2, mx) and np.allclose(lse2, mx + math.log(5))
+    # nothing selected
+    O3, mx3, lse3 = orc.mla_attention_into(q, np.zeros((0, 576)), tau)
+    assert np.all(O3 == 0) and np.all(np.isneginf(mx3)) and np.all(np.isneginf(lse3))
+    # splits: the largest split maximum is the maximum over the union
+    KV = rng.standard_normal((40, 576)) * 0.5
+    _, mxa, _ = orc.mla_attention_into(q, KV, tau)
+    parts = [orc.mla_attention_into(q, KV[p], tau)[1] for p in np.array_split(np.arange(40), 3)]
+    assert np.array_equal(np.max(np.stack(parts), axis=0), mxa)
+
+
 @pytest.mark.parametrize("S", [1, 2, 7, 64])
 def test_split_then_merge_equals_single_pass(S):
     rng = np.random.default_rng(7)
