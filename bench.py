@@ -59,9 +59,13 @@ def parse():
     ap.add_argument("--rows-per-req", type=int, default=None,
                     help="with --config: query rows per request at consecutive positions "
                          "(MTP verify or a multi-query extend)")
-    ap.add_argument("--kernel", default=None, choices=["indexer", "topk", "mla", "cache_write"],
+    ap.add_argument("--kernel", default=None,
+                    choices=["indexer", "topk", "mla", "cache_write", "prefill_into"],
                     help="time one kernel of the step alone on the same workload (a short "
-                         "run for profilers: W warm-up launches, then K timed ones)")
+                         "run for profilers: W warm-up launches, then K timed ones); "
+                         "prefill_into: the sparse attention of every query row into "
+                         "caller-owned O, max-logit and LSE (with --rows-per-req, a chunk of "
+                         "that many rows per request)")
     return ap.parse_args()
 
 
@@ -289,6 +293,8 @@ def run_kernel_only(args):
     dev = torch.device("cuda", 0)
     cfg = 1 if args.config is None else args.config
     kw = {"B": args.batch} if (cfg == 4 and args.batch) else {}
+    if args.rows_per_req:
+        kw["rows_per_req"] = args.rows_per_req
     spec = config_spec(cfg, **kw)
     if spec.shards > 1:
         raise SystemExit("--kernel times the unsharded path; configuration 3 is sharded")
@@ -311,6 +317,9 @@ def run_kernel_only(args):
                          dtype=torch.uint8, device=dev)
     if args.kernel == "cache_write":
         return time_cache_write(args, dw, spec, dev, err)
+    pre_ws = torch.empty(max(1, api.dsa_sparse_mla_prefill_into_workspace_size(R, H, k, 0)),
+                         dtype=torch.uint8, device=dev)
+    out_max = torch.empty(R, H, device=dev)
     fn = {
         "indexer": lambda: api.dsa_indexer_scores(dw.q_idx, dw.w_idx, dw.idx_k, dw.rows, scores,
                                                   err),
@@ -318,6 +327,9 @@ def run_kernel_only(args):
         "mla": lambda: api.dsa_sparse_mla_decode(dw.q, wl.sm_scale, dw.kv, dw.rows, tidx, tcnt,
                                                  out, lse, err, workspace=mla_ws,
                                                  num_splits=lay.num_splits),
+        "prefill_into": lambda: api.dsa_sparse_mla_prefill_into(
+            dw.q, wl.sm_scale, dw.kv, dw.rows, tidx, tcnt, out, out_max, lse, err,
+            workspace=pre_ws, num_splits=0),
     }[args.kernel]
     flush_w = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
@@ -335,8 +347,19 @@ def run_kernel_only(args):
             ms.append(a.elapsed_time(b))
     if api.dsa_read_error(err) != 0:
         raise SystemExit("device error word set")
-    print(json.dumps({"kernel": args.kernel, "workload": spec.name, "launches": args.steps,
-                      "us_mean": round(1e3 * float(np.mean(ms)), 2)}), flush=True)
+    line = {"kernel": args.kernel, "workload": spec.name, "launches": args.steps,
+            "us_mean": round(1e3 * float(np.mean(ms)), 2)}
+    if args.kernel in ("mla", "prefill_into"):
+        # rows attended per second, and the gathered latent rows' bytes per
+        # second (a row's selections overlap its neighbours' in a chunk, so
+        # part of them come from L2)
+        row_b = 576 * (1 if spec.dtype == "fp8_e4m3" else 2) + (4 if spec.dtype == "fp8_e4m3" else 0)
+        gathered = float(tcnt.sum().item()) * row_b
+        sec = float(np.mean(ms)) * 1e-3
+        line.update({"rows": R, "rows_per_req": spec.rows_per_req,
+                     "rows_per_s": round(R / sec, 1),
+                     "gathered_gbs": round(gathered / sec / 1e9, 1)})
+    print(json.dumps(line), flush=True)
 
 
 def time_cache_write(args, dw, spec, dev, err):

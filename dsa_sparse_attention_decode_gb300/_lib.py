@@ -115,6 +115,11 @@ PROTOTYPES = {
                                       POINTER(DsaRows), c_void_p, c_void_p, c_int32, c_int32,
                                       c_void_p, c_void_p, c_void_p, c_size_t, c_void_p,
                                       c_void_p]),
+    "dsa_sparse_mla_prefill_into_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32]),
+    "dsa_sparse_mla_prefill_into": (c_int, [c_void_p, c_int32, c_float, POINTER(DsaPagedCache),
+                                            POINTER(DsaRows), c_void_p, c_void_p, c_int32, c_int32,
+                                            c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                            c_void_p, c_void_p]),
     "dsa_sparse_mla_decode_noalloc": (c_int, [c_void_p, c_int32, c_float, POINTER(DsaPagedCache),
                                               POINTER(DsaRows), c_void_p, c_void_p, c_int32,
                                               c_int32, c_void_p, c_void_p, c_void_p, c_void_p]),

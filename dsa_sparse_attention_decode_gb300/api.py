@@ -153,6 +153,27 @@ def dsa_sparse_mla_decode(q, sm_scale: float, kv: PagedCache, rows: Rows, idx, c
            "dsa_sparse_mla_decode")
 
 
+def dsa_sparse_mla_prefill_into_workspace_size(num_rows: int, heads: int, k: int,
+                                               num_splits: int = 0) -> int:
+    return int(C.lib().dsa_sparse_mla_prefill_into_workspace_size(num_rows, heads, k, num_splits))
+
+
+def dsa_sparse_mla_prefill_into(q, sm_scale: float, kv: PagedCache, rows: Rows, idx, count, out,
+                                out_max_logit, out_lse, d_err, workspace=None,
+                                num_splits: int = 0, stream=None):
+    """Sparse attention of many query rows into caller-owned O, max-logit and
+    LSE buffers (see the header)."""
+    c, r = kv.c(), rows.c()
+    k = int(idx.shape[1])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(C.lib().dsa_sparse_mla_prefill_into(_ptr(q), int(q.shape[1]), float(sm_scale),
+                                               ctypes.byref(c), ctypes.byref(r), _ptr(idx),
+                                               _ptr(count), k, num_splits, _ptr(out),
+                                               _ptr(out_max_logit), _ptr(out_lse), _ptr(workspace),
+                                               ws_bytes, _ptr(d_err), _stream(stream)),
+           "dsa_sparse_mla_prefill_into")
+
+
 def dsa_sparse_mla_decode_noalloc(q, sm_scale: float, kv: PagedCache, rows: Rows, idx, count,
                                   out, out_lse, d_err, num_splits: int = 0, stream=None):
     """dsa_sparse_mla_decode for callers that cannot allocate device memory:

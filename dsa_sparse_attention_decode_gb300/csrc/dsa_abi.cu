@@ -132,6 +132,83 @@ cudaError_t make_index_k_tmap(CUtensorMap* map, const dsa_paged_cache& c) {
 
 using namespace dsa;
 
+namespace {
+
+// Workspace bytes of a sparse MLA call: the split-K partial outputs and LSEs,
+// and with_max the partial maxima (none with a single split)
+size_t mla_workspace_bytes(int32_t num_rows, int32_t heads, int32_t k, int32_t num_splits,
+                           bool with_max) {
+  if (num_rows < 0 || heads < 1 || k < 1 || num_splits < 0) return 0;
+  const int S = resolve_splits(num_splits, num_rows, k, k);
+  if (S <= 1) return 0;
+  const int64_t o = align_up(static_cast<int64_t>(S) * num_rows * heads * kVDim * 4, kAlign);
+  const int64_t l = align_up(static_cast<int64_t>(S) * num_rows * heads * 4, kAlign);
+  return static_cast<size_t>(o + l + (with_max ? l : 0));
+}
+
+// dsa_sparse_mla_decode, and with out_max != nullptr dsa_sparse_mla_prefill_into
+int run_sparse_mla(const uint16_t* q, int32_t heads, float sm_scale, const dsa_paged_cache* kv,
+                   const dsa_rows* rows, const int32_t* idx, const int32_t* count, int32_t k,
+                   int32_t num_splits, float* out, float* out_max, float* out_lse,
+                   void* workspace, size_t workspace_bytes, int32_t* d_err, void* stream) {
+  int st = check_rows(rows);
+  if (st != DSA_OK) return st;
+  st = check_cache(kv, kKvDim);
+  if (st != DSA_OK) return st;
+  if (heads != 16 && heads != 32) return DSA_ERR_UNSUPPORTED;
+  if (k < 1 || k > 4096 || num_splits < 0 || d_err == nullptr) return DSA_ERR_INVALID_ARG;
+  const int R = rows->num_rows;
+  if (R == 0) return DSA_OK;
+  if (!q || !idx || !count || !out || !out_lse || !aligned16(q) || !aligned16(out))
+    return DSA_ERR_INVALID_ARG;
+  const bool with_max = out_max != nullptr;
+  const int S = resolve_splits(num_splits, R, k, k);
+  const int chunk = split_chunk(S, k);
+  if (mla_smem_bytes(heads, kv->dtype == DSA_DTYPE_FP8_E4M3, chunk) > 227 * 1024)
+    return DSA_ERR_UNSUPPORTED;
+  const size_t need = mla_workspace_bytes(R, heads, k, num_splits, with_max);
+  if (workspace_bytes < need || (need > 0 && workspace == nullptr))
+    return DSA_ERR_WORKSPACE_TOO_SMALL;
+  if (static_cast<long long>(kv->num_pages) * kv->page_size > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+  MlaLaunch L{};
+  fill_mla_shard(L, 0, *kv);
+  L.page_size = kv->page_size;
+  L.fp8 = kv->dtype == DSA_DTYPE_FP8_E4M3;
+  L.nshards = 1;
+  L.q = q;
+  L.heads = heads;
+  L.sm_scale = sm_scale;
+  L.row_start = rows->row_start;
+  L.num_reqs = rows->num_reqs;
+  L.rows = R;
+  L.idx = idx;
+  L.count = count;
+  L.k = k;
+  L.num_splits = S;
+  L.chunk = chunk;
+  L.out = out;
+  L.out_lse = out_lse;
+  L.out_max = out_max;
+  L.d_err = d_err;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (S > 1) {
+    const int64_t o = align_up(static_cast<int64_t>(S) * R * heads * kVDim * 4, kAlign);
+    const int64_t l = align_up(static_cast<int64_t>(S) * R * heads * 4, kAlign);
+    L.part_out = reinterpret_cast<float*>(ws);
+    L.part_lse = reinterpret_cast<float*>(ws + o);
+    if (with_max) L.part_max = reinterpret_cast<float*>(ws + o + l);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_sparse_mla(L, s);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  if (S > 1)
+    e = launch_lse_merge(L.part_out, L.part_lse, S, R, heads, kVDim, out, out_lse, s, false,
+                         L.part_max, out_max);
+  return cuda_status(e);
+}
+
+}  // namespace
+
 extern "C" {
 
 int dsa_abi_version(void) { return DSA_ABI_VERSION; }
@@ -245,12 +322,7 @@ int dsa_shard_topk_merge(const float* cand_score, const int32_t* cand_pos,
 
 size_t dsa_sparse_mla_decode_workspace_size(int32_t num_rows, int32_t heads, int32_t k,
                                             int32_t num_splits) {
-  if (num_rows < 0 || heads < 1 || k < 1 || num_splits < 0) return 0;
-  const int S = resolve_splits(num_splits, num_rows, k, k);
-  if (S <= 1) return 0;
-  const int64_t o = align_up(static_cast<int64_t>(S) * num_rows * heads * kVDim * 4, kAlign);
-  const int64_t l = align_up(static_cast<int64_t>(S) * num_rows * heads * 4, kAlign);
-  return static_cast<size_t>(o + l);
+  return mla_workspace_bytes(num_rows, heads, k, num_splits, false);
 }
 
 int dsa_sparse_mla_decode(const uint16_t* q, int32_t heads, float sm_scale,
@@ -258,54 +330,24 @@ int dsa_sparse_mla_decode(const uint16_t* q, int32_t heads, float sm_scale,
                           const int32_t* count, int32_t k, int32_t num_splits, float* out,
                           float* out_lse, void* workspace, size_t workspace_bytes,
                           int32_t* d_err, void* stream) {
-  int st = check_rows(rows);
-  if (st != DSA_OK) return st;
-  st = check_cache(kv, kKvDim);
-  if (st != DSA_OK) return st;
-  if (heads != 16 && heads != 32) return DSA_ERR_UNSUPPORTED;
-  if (k < 1 || k > 4096 || num_splits < 0 || d_err == nullptr) return DSA_ERR_INVALID_ARG;
-  const int R = rows->num_rows;
-  if (R == 0) return DSA_OK;
-  if (!q || !idx || !count || !out || !out_lse || !aligned16(q) || !aligned16(out))
-    return DSA_ERR_INVALID_ARG;
-  const int S = resolve_splits(num_splits, R, k, k);
-  const int chunk = split_chunk(S, k);
-  if (mla_smem_bytes(heads, kv->dtype == DSA_DTYPE_FP8_E4M3, chunk) > 227 * 1024)
-    return DSA_ERR_UNSUPPORTED;
-  const size_t need = dsa_sparse_mla_decode_workspace_size(R, heads, k, num_splits);
-  if (workspace_bytes < need || (need > 0 && workspace == nullptr))
-    return DSA_ERR_WORKSPACE_TOO_SMALL;
-  if (static_cast<long long>(kv->num_pages) * kv->page_size > INT32_MAX) return DSA_ERR_UNSUPPORTED;
-  MlaLaunch L{};
-  fill_mla_shard(L, 0, *kv);
-  L.page_size = kv->page_size;
-  L.fp8 = kv->dtype == DSA_DTYPE_FP8_E4M3;
-  L.nshards = 1;
-  L.q = q;
-  L.heads = heads;
-  L.sm_scale = sm_scale;
-  L.row_start = rows->row_start;
-  L.num_reqs = rows->num_reqs;
-  L.rows = R;
-  L.idx = idx;
-  L.count = count;
-  L.k = k;
-  L.num_splits = S;
-  L.chunk = chunk;
-  L.out = out;
-  L.out_lse = out_lse;
-  L.d_err = d_err;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (S > 1) {
-    L.part_out = reinterpret_cast<float*>(ws);
-    L.part_lse = reinterpret_cast<float*>(
-        ws + align_up(static_cast<int64_t>(S) * R * heads * kVDim * 4, kAlign));
-  }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_sparse_mla(L, s);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
-  if (S > 1) e = launch_lse_merge(L.part_out, L.part_lse, S, R, heads, kVDim, out, out_lse, s);
-  return cuda_status(e);
+  return run_sparse_mla(q, heads, sm_scale, kv, rows, idx, count, k, num_splits, out, nullptr,
+                        out_lse, workspace, workspace_bytes, d_err, stream);
+}
+
+size_t dsa_sparse_mla_prefill_into_workspace_size(int32_t num_rows, int32_t heads, int32_t k,
+                                                  int32_t num_splits) {
+  return mla_workspace_bytes(num_rows, heads, k, num_splits, true);
+}
+
+int dsa_sparse_mla_prefill_into(const uint16_t* q, int32_t heads, float sm_scale,
+                                const dsa_paged_cache* kv, const dsa_rows* rows,
+                                const int32_t* idx, const int32_t* count, int32_t k,
+                                int32_t num_splits, float* out, float* out_max_logit,
+                                float* out_lse, void* workspace, size_t workspace_bytes,
+                                int32_t* d_err, void* stream) {
+  if (rows != nullptr && rows->num_rows > 0 && out_max_logit == nullptr) return DSA_ERR_INVALID_ARG;
+  return run_sparse_mla(q, heads, sm_scale, kv, rows, idx, count, k, num_splits, out,
+                        out_max_logit, out_lse, workspace, workspace_bytes, d_err, stream);
 }
 
 int dsa_lse_merge(const float* O_parts, const float* lse_parts, int32_t num_parts,

@@ -111,6 +111,8 @@ struct MlaLaunch {
   float* out_lse;
   float* part_out;         // else: part p = w * S + s at part_out + p*R*H*512
   float* part_lse;
+  float* out_max;          // optional max scaled logit [R][H] (nullptr: not written)
+  float* part_max;         // with it and parts > 1: part p at part_max + p*R*H
   int32_t* d_err;
 };
 // pdl: the kernel reads the query, row_start and block tables before it waits
@@ -142,9 +144,12 @@ cudaError_t launch_cache_write(const CacheWriteLaunch& p, cudaStream_t stream);
 
 // ------------------------------------------------------------- LSE merge
 
+// max_parts / out_max (optional, both or neither): out_max = the largest of
+// the parts' maxima, per (row, head)
 cudaError_t launch_lse_merge(const float* O_parts, const float* lse_parts, int parts,
                              int rows, int heads, int dv, float* out, float* out_lse,
-                             cudaStream_t stream, bool pdl = false);
+                             cudaStream_t stream, bool pdl = false,
+                             const float* max_parts = nullptr, float* out_max = nullptr);
 
 int num_sms();
 

@@ -197,7 +197,8 @@ constexpr int kFastParts = 8;
 __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
                                  const float* __restrict__ lse_parts, int parts, int rows,
                                  int heads, int dv, float* __restrict__ out,
-                                 float* __restrict__ out_lse) {
+                                 float* __restrict__ out_lse, const float* __restrict__ max_parts,
+                                 float* __restrict__ out_max) {
   const int rh = blockIdx.x;  // r * heads + h
   pdl_trigger();
   pdl_wait();  // the partials come from the previous grid
@@ -255,6 +256,12 @@ __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
     reinterpret_cast<float4*>(out + static_cast<long long>(rh) * dv)[d4] =
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   if (threadIdx.x == 0) out_lse[rh] = m == kNegInf ? m : m + logf(den);
+  // the largest scaled logit over the parts (an empty part holds -inf)
+  if (out_max != nullptr && threadIdx.x == 0) {
+    float mx = kNegInf;
+    for (int p = 0; p < parts; ++p) mx = fmaxf(mx, __ldcg(max_parts + p * stride_p + rh));
+    out_max[rh] = mx;
+  }
 }
 
 }  // namespace
@@ -273,12 +280,13 @@ cudaError_t launch_shard_topk_merge(const MergeTopkLaunch& p, cudaStream_t strea
 
 cudaError_t launch_lse_merge(const float* O_parts, const float* lse_parts, int parts, int rows,
                              int heads, int dv, float* out, float* out_lse, cudaStream_t stream,
-                             bool pdl) {
+                             bool pdl, const float* max_parts, float* out_max) {
   if (rows * heads == 0) return cudaSuccess;
   if (dv % 4 != 0 || dv / 4 > 1024) return cudaErrorInvalidValue;
   const int threads = ((dv / 4 + 31) / 32) * 32;  // one float4 of the value dims per thread
+  if ((max_parts == nullptr) != (out_max == nullptr)) return cudaErrorInvalidValue;
   return launch_ex(lse_merge_kernel, dim3(rows * heads), dim3(threads), 0, stream, pdl, O_parts,
-                   lse_parts, parts, rows, heads, dv, out, out_lse);
+                   lse_parts, parts, rows, heads, dv, out, out_lse, max_parts, out_max);
 }
 
 }  // namespace dsa

@@ -219,8 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
                         : P.part_out + (static_cast<long long>(part) * P.rows + r) * H * kVDim;
   float* out_l = direct ? P.out_lse + static_cast<long long>(r) * H
                         : P.part_lse + (static_cast<long long>(part) * P.rows + r) * H;
+  // the largest scaled logit, when the caller asks for it
+  float* out_m = P.out_max == nullptr ? nullptr
+                 : direct ? P.out_max + static_cast<long long>(r) * H
+                          : P.part_max + (static_cast<long long>(part) * P.rows + r) * H;
   if (ntok == 0) {
-    for (int h = tid; h < H; h += kThreads) out_l[h] = -__int_as_float(0x7f800000);
+    for (int h = tid; h < H; h += kThreads) {
+      out_l[h] = -__int_as_float(0x7f800000);
+      if (out_m) out_m[h] = -__int_as_float(0x7f800000);
+    }
     if (direct)
       for (int i = tid; i < H * kVDim; i += kThreads) out_o[i] = 0.0f;
     if (!kFp8 && tid < kCompute) cp_async_wait<0>();  // no copy may land after the CTA leaves
@@ -618,6 +625,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaLaunch
         }
         if (wg == 0 && t4 == 0) {
           out_l[h] = l > 0.0f ? (m_run[a][hh] + log2f(l)) * kLn2 : -__int_as_float(0x7f800000);
+          // m_run is the largest logit in base 2 (tau * q.kv * log2 e)
+          if (out_m) out_m[h] = l > 0.0f ? m_run[a][hh] * kLn2 : -__int_as_float(0x7f800000);
         }
       }
     }

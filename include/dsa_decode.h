@@ -275,6 +275,42 @@ int dsa_sparse_mla_decode(const uint16_t* q, int32_t heads, float sm_scale,
                           int32_t* d_err, void* stream);
 
 /*
+ * Workspace bytes dsa_sparse_mla_prefill_into needs for these sizes (num_splits
+ * 0 = the automatic choice on the current device): the split-K partial
+ * outputs, LSEs and maxima; 0 with a single split.
+ */
+size_t dsa_sparse_mla_prefill_into_workspace_size(int32_t num_rows, int32_t heads,
+                                                  int32_t k, int32_t num_splits);
+
+/*
+ * dsa_sparse_mla_prefill_into -- sparse attention of many query rows (a
+ * prefill or extend chunk: each row with its own selected positions, e.g.
+ * from dsa_topk over its causal prefix) that writes all three outputs into
+ * caller-owned buffers (DSpark page, section 6.3 "Reserve sparse-prefill
+ * outputs before allocator fragmentation": the output, max-logit and LSE
+ * tensors are reserved once by the caller and the kernel writes into them).
+ * Nothing is allocated; the split-K partials go to the caller's workspace.
+ *
+ * Same arguments, checks and errors as dsa_sparse_mla_decode, plus:
+ *   out_max_logit: device fp32 [num_rows][heads], the largest scaled logit
+ *             sm_scale * q.kv over the row's selected rows (natural units,
+ *             not exponentiated); -inf for an empty row.  Required: NULL with
+ *             num_rows > 0 is DSA_ERR_INVALID_ARG.  For every row,
+ *             out_lse - ln(count) <= out_max_logit <= out_lse.
+ *   workspace: device, >= dsa_sparse_mla_prefill_into_workspace_size() bytes
+ *             (may be NULL when that size is 0); DSA_ERR_WORKSPACE_TOO_SMALL
+ *             otherwise, before any launch.
+ * Rows of one request are independent here: each reads only its own list
+ * idx[r][0 .. count[r]) through its request's block table.
+ */
+int dsa_sparse_mla_prefill_into(const uint16_t* q, int32_t heads, float sm_scale,
+                                const dsa_paged_cache* kv, const dsa_rows* rows,
+                                const int32_t* idx, const int32_t* count, int32_t k,
+                                int32_t num_splits, float* out, float* out_max_logit,
+                                float* out_lse, void* workspace, size_t workspace_bytes,
+                                int32_t* d_err, void* stream);
+
+/*
  * Size of the fixed device array behind dsa_sparse_mla_decode_noalloc.
  */
 #define DSA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)

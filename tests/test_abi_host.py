@@ -87,6 +87,34 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert st == C.DSA_ERR_UNSUPPORTED
 
 
+def test_prefill_into_host_checks(lib):
+    """The sparse-prefill entry point's caller-owned contract, without a GPU:
+    the max-logit buffer is required, the workspace holds the partial maxima
+    beside the partial outputs and LSEs, and a short workspace is refused
+    before any launch."""
+    err = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    cache = C.DsaPagedCache(data=16, scale=None, block_table=None, dtype=0, row_elems=576,
+                            page_size=64, num_pages=64, max_blocks=64)
+    rows = C.DsaRows(num_rows=3, num_reqs=1, max_rows_per_req=3, max_len=4096, row_start=16,
+                     row_pos=16)
+    args = (ctypes.c_void_p(16), 32, 0.1, ctypes.byref(cache), ctypes.byref(rows),
+            ctypes.c_void_p(16), ctypes.c_void_p(16), 2048, 4, ctypes.c_void_p(16))
+    # no max-logit buffer
+    assert lib.dsa_sparse_mla_prefill_into(*args, None, ctypes.c_void_p(16), None, 0, err,
+                                           None) == C.DSA_ERR_INVALID_ARG
+    # 4 splits: decode's partials plus 4 x rows x heads maxima (256-byte aligned)
+    dec = lib.dsa_sparse_mla_decode_workspace_size(3, 32, 2048, 4)
+    pre = lib.dsa_sparse_mla_prefill_into_workspace_size(3, 32, 2048, 4)
+    assert dec > 0 and pre - dec == -(-(4 * 3 * 32 * 4) // 256) * 256
+    assert lib.dsa_sparse_mla_prefill_into_workspace_size(3, 32, 2048, 1) == 0
+    assert lib.dsa_sparse_mla_prefill_into(*args, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                           ctypes.c_void_p(256), pre - 1, err,
+                                           None) == C.DSA_ERR_WORKSPACE_TOO_SMALL
+    # zero rows: nothing to do
+    rows.num_rows = 0
+    assert lib.dsa_sparse_mla_prefill_into(*args, None, None, None, 0, err, None) == C.DSA_OK
+
+
 def test_decode_workspace_layout_host_only(lib):
     ik = (C.DsaPagedCache * 2)(
         *[C.DsaPagedCache(data=16, scale=None, block_table=None, dtype=0, row_elems=128,

@@ -215,6 +215,48 @@ def test_sparse_mla_alone(cfg):
             assert eo <= (2e-3 if cfg == 1 else 5e-3) and el <= 1e-4, (S, r, eo, el)
 
 
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_sparse_mla_prefill_into(cfg):
+    """Sparse attention of a prefill chunk (two requests of 40 query rows at
+    consecutive positions, each row with its own selection from its causal
+    prefix, some empty) into caller-owned O, max-logit and LSE buffers."""
+    wl = make_workload(config_spec(cfg, B=2, L=3000, L_lo=2500, L_hi=4000, rows_per_req=40))
+    dw = upload(wl, DEV)
+    rng = np.random.default_rng(31)
+    k = 2048
+    idx = np.full((wl.R, k), -1, np.int32)
+    cnt = np.zeros(wl.R, np.int32)
+    for r in range(wl.R):
+        n = [2048, 0, 1, 700, 2048, 64, 65, 1000, 3, 2047][r % 10]
+        n = min(n, int(wl.row_pos[r]) + 1)
+        idx[r, :n] = np.sort(rng.choice(int(wl.row_pos[r]) + 1, n, replace=False))
+        cnt[r] = n
+    t = lambda a: torch.from_numpy(a).to(DEV)  # noqa: E731
+    for S in (0, 1, 3):
+        out = torch.full((wl.R, wl.H, 512), 7.0, device=DEV)
+        mx = torch.full((wl.R, wl.H), 7.0, device=DEV)
+        lse = torch.full((wl.R, wl.H), 7.0, device=DEV)
+        wsz = api.dsa_sparse_mla_prefill_into_workspace_size(wl.R, wl.H, k, S)
+        ws = torch.zeros(max(wsz, 1), dtype=torch.uint8, device=DEV)
+        err = _err()
+        api.dsa_sparse_mla_prefill_into(dw.q, wl.sm_scale, dw.kv, dw.rows, t(idx), t(cnt), out,
+                                        mx, lse, err, workspace=ws, num_splits=S)
+        assert api.dsa_read_error(err) == 0
+        O_all, m_all, l_all = out.cpu().numpy(), mx.cpu().numpy(), lse.cpu().numpy()
+        for r in range(wl.R):
+            O_ref, m_ref, l_ref = orc.row_attention_into(wl, r, idx[r, : cnt[r]])
+            if cnt[r] == 0:
+                assert np.all(O_all[r] == 0) and np.all(np.isneginf(m_all[r]))
+                assert np.all(np.isneginf(l_all[r]))
+                continue
+            eo, el = attn_err(O_all[r], l_all[r], O_ref, l_ref)
+            assert eo <= (2e-3 if cfg == 1 else 5e-3) and el <= 1e-4, (S, r, eo, el)
+            assert np.max(np.abs(m_all[r] - m_ref)) <= 1e-4, (S, r)
+            # the bound the three outputs satisfy together
+            assert np.all(m_all[r] <= l_all[r] + 1e-5)
+            assert np.all(m_all[r] >= l_all[r] - np.log(cnt[r]) - 1e-5)
+
+
 @pytest.mark.parametrize("cfg", [0, 1])
 def test_sparse_mla_running_max_moves(cfg):
     """Selected rows scaled by 1, 10 and 30 tile by tile (64 tokens, in list
