@@ -215,7 +215,7 @@ def test_sparse_mla_alone(cfg):
             assert eo <= (2e-3 if cfg == 1 else 5e-3) and el <= 1e-4, (S, r, eo, el)
 
 
-@pytest.mark.parametrize("cfg", [1, 2])
+@pytest.mark.parametrize("cfg", [0, 1, 2])
 def test_sparse_mla_prefill_into(cfg):
     """Sparse attention of a prefill chunk (two requests of 40 query rows at
     consecutive positions, each row with its own selection from its causal
@@ -250,7 +250,7 @@ def test_sparse_mla_prefill_into(cfg):
                 assert np.all(np.isneginf(l_all[r]))
                 continue
             eo, el = attn_err(O_all[r], l_all[r], O_ref, l_ref)
-            assert eo <= (2e-3 if cfg == 1 else 5e-3) and el <= 1e-4, (S, r, eo, el)
+            assert eo <= (5e-3 if cfg == 2 else 2e-3) and el <= 1e-4, (S, r, eo, el)
             assert np.max(np.abs(m_all[r] - m_ref)) <= 1e-4, (S, r)
             # the bound the three outputs satisfy together
             assert np.all(m_all[r] <= l_all[r] + 1e-5)
