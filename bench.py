@@ -109,7 +109,8 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "_build", f"clocks_{os.getpid()}.csv")
+        # the sampled clocks of this run (a git-ignored build folder)
+        self.path = os.path.join(ROOT, "_build", f"clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
