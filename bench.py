@@ -1,15 +1,20 @@
 #!/usr/bin/env python
 """Benchmark of the DSA sparse-attention decode path on GB300.
 
-Workload: batched decode, B = 32 requests x 1 query row, 32768 cached tokens
-each, bf16 caches, 64 x 128 indexer, 32 MLA heads x 576-wide latent rows,
-top-2048, 64-token pages with seeded random block tables (synthetic data).
+Default workload: the ragged throughput sweep's largest batch, B = 256
+requests x 1 query row, per-request cached length drawn log-uniform in
+[4K, 128K], fp8_e4m3 index keys and latent rows with one fp32 scale per token,
+64 x 128 indexer, 32 MLA heads x 576-wide latent rows, top-2048, 64-token
+pages with seeded random block tables (synthetic data).  `--config N`
+(`--batch B` for configuration 4) selects another configuration of the
+same contract line.
 
 A step is one dsa_decode call (indexer -> top-k -> sparse MLA split-K ->
 LSE merge) over the whole batch, inputs resident in HBM.  Between timed steps
 L2 is flushed by writing a 512 MB buffer and then reading a 256 MB one (the
-step's own HBM stream, ~350 MB, is also larger than L2).  Each step is timed with CUDA events on the launching
-stream; `value` = rows of all ranks / max over ranks of the summed step time.
+step's own HBM stream is also larger than L2 for every configuration but the
+tiny one).  Each step is timed with CUDA events on the launching stream;
+`value` = rows of all ranks / max over ranks of the summed step time.
 
 `--impl reference` times the CPU oracle instead (the only other place that
 runs it is the `cpu_baseline` leg): same workload, same metric, each step a
@@ -38,8 +43,8 @@ import numpy as np  # noqa: E402
 
 METRIC = "DSA decode query-rows/sec at 1 GB300; HBM GB/s as fraction of ~8 TB/s roofline"
 UNIT = "rows/s"
-WORKLOAD = ("decode B=32 x 1 row, L=32768, bf16 paged caches (page 64, random block tables), "
-            "indexer 64x128, MLA 32 heads x 576, top-2048")
+DEFAULT_CONFIG = 4
+DEFAULT_BATCH = 256
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -51,13 +56,15 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="product", choices=["product", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg (host copies through the C ABI)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--config", type=int, default=None,
-                    help="time the fused step on configuration 0..4 instead (device time only, "
-                         "one JSON line; the contract line is the default configuration 1)")
-    ap.add_argument("--batch", type=int, default=None, help="requests of configuration 4")
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG,
+                    help="workload: configuration 0..4 (default 4, the ragged fp8 sweep)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help=f"requests of configuration 4 (default {DEFAULT_BATCH})")
     ap.add_argument("--rows-per-req", type=int, default=None,
-                    help="with --config: query rows per request at consecutive positions "
+                    help="query rows per request at consecutive positions "
                          "(MTP verify or a multi-query extend)")
     ap.add_argument("--kernel", default=None,
                     choices=["indexer", "topk", "mla", "cache_write", "prefill_into"],
@@ -67,6 +74,37 @@ def parse():
                          "caller-owned O, max-logit and LSE (with --rows-per-req, a chunk of "
                          "that many rows per request)")
     return ap.parse_args()
+
+
+def workload_spec(args):
+    from workloads import config_spec
+
+    kw = {}
+    if args.config == 4:
+        kw["B"] = args.batch or DEFAULT_BATCH
+    elif args.batch:
+        kw["B"] = args.batch
+    if args.rows_per_req:
+        kw["rows_per_req"] = args.rows_per_req
+    return config_spec(args.config, **kw)
+
+
+def describe(wl) -> dict:
+    """The workload's name and shape for the JSON line's `config`."""
+    s = wl.spec
+    L = wl.seq_len
+    law = (f"L={int(L[0])}" if s.length_law == "fixed" and s.seq_lens is None else
+           f"L {s.length_law} in [{s.L_lo}, {s.L_hi}] (drawn: min {int(L.min())}, "
+           f"mean {float(L.mean()):.0f}, max {int(L.max())})")
+    store = "bf16" if s.dtype == "bf16" else "fp8_e4m3 (one fp32 scale per token)"
+    paging = "page 64, random block tables" if s.paged else "contiguous"
+    text = (f"{s.name}: decode B={s.B} x {s.rows_per_req} row(s), {law}, {store} index-K and "
+            f"latent caches ({paging}), indexer 64x128, MLA {s.H} heads x 576, "
+            f"top-{s.topk}" + (f", W={s.shards} token shards emulated on one GPU"
+                               if s.shards > 1 else ""))
+    return {"workload": text, "global_batch": int(wl.R), "seq_len_mean": float(L.mean()),
+            "seq_len_max": int(L.max()), "kv_dtype": s.dtype, "topk": s.topk,
+            "mla_heads": s.H, "shards": s.shards}
 
 
 # ----------------------------------------------------------------- ranks
@@ -188,94 +226,54 @@ def kernel_source_hash(names):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source."""
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summaries, if one was
+    taken of this kernel on this workload with the current kernel source."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
-            d = json.load(f)[kernel]
+            entries = json.load(f)
     except Exception:
         return None
-    if d.get("source_hash") != kernel_source_hash(d.get("sources", [])):
-        return None
-    return d.get("dram_bytes_per_launch")
+    for d in entries:
+        if d.get("kernel") != kernel or d.get("workload") != workload:
+            continue
+        if d.get("source_hash") != kernel_source_hash(d.get("sources", [])):
+            return None
+        return d.get("dram_bytes_per_launch")
+    return None
 
 
 def algorithmic_bytes(wl):
-    """Bytes the method must move per step:
-    indexer key stream + block table + queries/weights; MLA selected rows +
-    indices + query + output/LSE."""
+    """Bytes the method must move per step, per kernel:
+    indexer: key stream (+ fp8 scales) + block tables + queries/weights;
+    top-k: the valid scores read + the selection written;
+    MLA (+ LSE merge): selected latent rows (+ fp8 scales) + indices + query
+    + output/LSE; with W shards also the W partials the merge reads and the
+    result it writes (H * 513 * 4 B each)."""
     R, H = wl.R, wl.H
     k = wl.topk
-    esz_k = 2 if wl.spec.dtype == "bf16" else 1
-    per_tok_idx = 128 * esz_k + (0 if esz_k == 2 else 4)
-    per_tok_kv = 576 * esz_k + (0 if esz_k == 2 else 4)
+    W = max(1, wl.W)
+    esz = 2 if wl.spec.dtype == "bf16" else 1
+    per_tok_idx = 128 * esz + (0 if esz == 2 else 4)
+    per_tok_kv = 576 * esz + (0 if esz == 2 else 4)
     idx = 0
     for b in range(wl.B):
         L = int(wl.row_pos[wl.row_start[b + 1] - 1]) + 1
         idx += L * per_tok_idx + ((L + 63) // 64) * 4
     idx += R * (64 * 128 * 2 + 64 * 4)
+    topk = 0
     mla = 0
     for r in range(R):
-        n = min(k, int(wl.row_pos[r]) + 1)
+        valid = int(wl.row_pos[r]) + 1
+        n = min(k, valid)
+        topk += valid * 4 + k * 4 + 4
         mla += n * per_tok_kv + k * 4 + H * 576 * 2 + H * 512 * 4 + H * 4
-    return idx, mla
+        if W > 1:
+            mla += (W + 1) * H * 513 * 4
+    return {"indexer": idx, "topk": topk, "mla": mla}
 
 
 # ----------------------------------------------------------------- product arm
-
-
-def run_config(args):
-    """The fused step on another configuration: `warmup` untimed steps, then
-    `steps` timed ones (CUDA events, L2 flushed before each)."""
-    import torch
-
-    import dsa_sparse_attention_decode_gb300 as pkg
-    from dsa_sparse_attention_decode_gb300 import api
-    from workloads import config_spec, make_workload
-    from workloads.device import decode_args, upload
-
-    pkg.build()
-    pkg.lib()
-    dev = torch.device("cuda", 0)
-    kw = {"B": args.batch} if (args.config == 4 and args.batch) else {}
-    if args.rows_per_req:
-        kw["rows_per_req"] = args.rows_per_req
-    spec = config_spec(args.config, **kw)
-    wl = make_workload(spec)
-    dw = upload(wl, dev, shards=spec.shards > 1, unsharded=spec.shards == 1)
-    R, H, k = wl.R, wl.H, wl.topk
-    out = torch.empty(R, H, 512, device=dev)
-    lse = torch.empty(R, H, device=dev)
-    desc = decode_args(dw, spec.shards > 1, out, lse)
-    ws = torch.zeros(max(1, api.dsa_decode_workspace_size(desc)), dtype=torch.uint8, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush_w = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
-    ms = []
-    for i in range(args.warmup + args.steps):
-        flush_w.zero_()
-        flush_r.sum()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
-        api.dsa_decode(desc, ws, err)
-        b.record()
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            ms.append(a.elapsed_time(b))
-    if api.dsa_read_error(err) != 0:
-        raise SystemExit("device error word set")
-    sec = float(np.mean(ms)) / 1e3
-    idx_b, mla_b = algorithmic_bytes(wl)
-    peaks, kind = measured_peaks()
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    gbs = (idx_b + mla_b) / sec / 1e9
-    print(json.dumps({"config": spec.name, "rows": R, "rows_per_req": spec.rows_per_req, "shards": spec.shards,
-                      "ms_per_step": round(sec * 1e3, 4), "rows_per_s": round(R / sec, 1),
-                      "algorithmic_bytes": idx_b + mla_b, "path_gbs": round(gbs, 1),
-                      "path_frac_of_measured": round(gbs / hbm, 4), "peak_source": kind}),
-          flush=True)
 
 
 def run_kernel_only(args):
@@ -286,17 +284,13 @@ def run_kernel_only(args):
 
     import dsa_sparse_attention_decode_gb300 as pkg
     from dsa_sparse_attention_decode_gb300 import api
-    from workloads import config_spec, make_workload
+    from workloads import make_workload
     from workloads.device import decode_args, upload
 
     pkg.build()
     pkg.lib()
     dev = torch.device("cuda", 0)
-    cfg = 1 if args.config is None else args.config
-    kw = {"B": args.batch} if (cfg == 4 and args.batch) else {}
-    if args.rows_per_req:
-        kw["rows_per_req"] = args.rows_per_req
-    spec = config_spec(cfg, **kw)
+    spec = workload_spec(args)
     if spec.shards > 1:
         raise SystemExit("--kernel times the unsharded path; configuration 3 is sharded")
     wl = make_workload(spec)
@@ -419,20 +413,21 @@ def run_product(args):
 
     import dsa_sparse_attention_decode_gb300 as pkg
     from dsa_sparse_attention_decode_gb300 import api
-    from workloads import config_spec, make_workload
+    from workloads import make_workload
     from workloads.device import decode_args, upload
 
     pkg.build()
     pkg.lib()
-    spec = config_spec(1)
+    spec = workload_spec(args)
+    sharded = spec.shards > 1
     wl = make_workload(spec)
-    dw = upload(wl, dev)
+    dw = upload(wl, dev, shards=sharded, unsharded=not sharded)
     R, H, k = wl.R, wl.H, wl.topk
     out = torch.empty(R, H, 512, device=dev)
     lse = torch.empty(R, H, device=dev)
     tidx = torch.empty(R, k, dtype=torch.int32, device=dev)
     tcnt = torch.empty(R, dtype=torch.int32, device=dev)
-    desc = decode_args(dw, False, out, lse, tidx, tcnt)
+    desc = decode_args(dw, sharded, out, lse, tidx, tcnt)
     lay = api.dsa_decode_workspace_layout(desc)
     ws = torch.zeros(lay.total_bytes, dtype=torch.uint8, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -483,26 +478,42 @@ def run_product(args):
     value, max_sec, total_rows = aggregate(R * args.steps, step_sec, device=dev)
     ms_per_step = max_sec * 1e3 / args.steps
 
-    # ---- per-kernel timing of the same path (live, CUDA events, same stream)
-    scores = ws[lay.scores: lay.scores + R * lay.ld_scores * 4].view(torch.float32).view(R, lay.ld_scores)
-    valid = (dw.rows.row_pos + 1).to(torch.int32)
-    kern = {}
-    kern["indexer"] = timed(lambda: api.dsa_indexer_scores(dw.q_idx, dw.w_idx, dw.idx_k, dw.rows,
-                                                          scores, err, stream=stream), args.steps)
-    kern["topk"] = timed(lambda: api.dsa_topk(scores, valid, k, tidx, tcnt, err, stream=stream),
-                         args.steps)
-    mla_ws = torch.empty(max(1, api.dsa_sparse_mla_decode_workspace_size(R, H, k, lay.num_splits)),
-                         dtype=torch.uint8, device=dev)
-    kern["sparse_mla+lse_merge"] = timed(
-        lambda: api.dsa_sparse_mla_decode(dw.q, wl.sm_scale, dw.kv, dw.rows, tidx, tcnt, out, lse,
-                                          err, workspace=mla_ws, num_splits=lay.num_splits,
-                                          stream=stream), args.steps)
-    torch.cuda.synchronize()
-    if api.dsa_read_error(err) != 0:
-        raise SystemExit("device error word set")
-    # median: one launch delayed by the host (the events bracket it) must not
-    # skew the per-kernel figures
-    kern_us = {n: 1e3 * float(np.median(v)) for n, v in kern.items()}
+    # ---- per-kernel timing of the same path (live, CUDA events, same stream),
+    # through the single-step entry points on the step's own intermediates
+    alg = algorithmic_bytes(wl)
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    kern_us = {}
+    if not sharded:
+        scores = ws[lay.scores: lay.scores + R * lay.ld_scores * 4].view(torch.float32).view(
+            R, lay.ld_scores)
+        valid = (dw.rows.row_pos + 1).to(torch.int32)
+        kern = {}
+        kern["indexer"] = timed(lambda: api.dsa_indexer_scores(
+            dw.q_idx, dw.w_idx, dw.idx_k, dw.rows, scores, err, stream=stream), args.steps)
+        kern["topk"] = timed(lambda: api.dsa_topk(scores, valid, k, tidx, tcnt, err,
+                                                  stream=stream), args.steps)
+        mla_ws = torch.empty(max(1, api.dsa_sparse_mla_decode_workspace_size(
+            R, H, k, lay.num_splits)), dtype=torch.uint8, device=dev)
+        kern["mla"] = timed(lambda: api.dsa_sparse_mla_decode(
+            dw.q, wl.sm_scale, dw.kv, dw.rows, tidx, tcnt, out, lse, err, workspace=mla_ws,
+            num_splits=lay.num_splits, stream=stream), args.steps)
+        torch.cuda.synchronize()
+        if api.dsa_read_error(err) != 0:
+            raise SystemExit("device error word set")
+        # median: one launch delayed by the host (the events bracket it) must
+        # not skew the per-kernel figures
+        kern_us = {n: 1e3 * float(np.median(v)) for n, v in kern.items()}
+    kernel_names = {"indexer": "indexer_kernel (dsa_indexer_scores)",
+                    "topk": "topk_kernel (dsa_topk)",
+                    "mla": "sparse_mla_kernel + lse_merge_kernel (dsa_sparse_mla_decode)"}
+    kernels = {}
+    for n, us in kern_us.items():
+        gbs = alg[n] / (us * 1e-6) / 1e9
+        kernels[n] = {"us": round(us, 2), "algorithmic_bytes": alg[n], "gbs": round(gbs, 1),
+                      "frac_of_measured_hbm": round(gbs / hbm, 4)}
+    if "topk" in kernels:
+        kernels["topk"]["note"] = "reads the indexer's scores from L2 where they fit"
 
     # ---- end to end through the C ABI with host buffers.  Every step copies
     # its inputs (queries, weights, row metadata, block tables) from one pinned
@@ -513,14 +524,83 @@ def run_product(args):
     # input copy of step i + 1 runs on one copy stream and the result copy of
     # step i - 1 on another while step i computes, ordered by events.  One
     # timed region spans all steps, from the first input copy to the last
-    # result copy (no L2 flush inside it: every step streams ~350 MB of
-    # caches, more than the 129 MB L2).
+    # result copy (no L2 flush inside it: every step streams its caches,
+    # more than the 129 MB L2 for every configuration but the tiny one).
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_leg(args, api, dw, wl, sharded, ws, err, stream, out, lse, tidx, tcnt, dev)
+
+    # ---- roofline of the dominant kernel (the longest one of the step)
+    path_bytes = sum(alg.values())
+    path_gbs = path_bytes / (ms_per_step * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "peak": hbm, "unit": "GB/s", "peak_source": peak_kind,
+                "path_algorithmic_bytes_per_step": path_bytes,
+                "path_achieved_gbs": round(path_gbs, 1),
+                "path_frac": round(path_gbs / hbm, 4),
+                "path_frac_of_nominal_8tbs": round(path_gbs / NOMINAL_HBM_GBS, 4)}
+    if kern_us:
+        dom = max(("indexer", "mla"), key=lambda n: kern_us[n])
+        ach = alg[dom] / (kern_us[dom] * 1e-6) / 1e9
+        roofline.update({"kernel": kernel_names[dom], "achieved": round(ach, 1),
+                         "frac": round(ach / hbm, 4), "algorithmic_bytes_per_launch": alg[dom],
+                         "traffic": ncu_traffic(dom, spec.name)})
+    else:
+        roofline.update({"kernel": "whole dsa_decode step (sharded: no single-kernel timing)",
+                         "achieved": round(path_gbs, 1), "frac": round(path_gbs / hbm, 4),
+                         "algorithmic_bytes_per_launch": path_bytes, "traffic": None})
+
+    # ---- CPU oracle baseline on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    if rank == 0:
+        launches_per_step = 3 + (1 if lay.num_parts > 1 else 0) + (1 if sharded else 0)
+        cfg = describe(wl)
+        cfg["parallelism"] = f"dp{world} (independent request batches per GPU)"
+        cfg["l2"] = ("flushed between timed steps (512 MB write, then 256 MB read); "
+                     f"the step streams {path_bytes / 1e6:.0f} MB")
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8_e4m3 caches, fp32 accumulate" if spec.dtype != "bf16" else "bf16",
+            "data": "synthetic (seeded N(0,1)/N(0,0.5) caches and queries, U(0,1)/8 weights)",
+            "config": cfg,
+            "roofline": roofline,
+            "num_splits": lay.num_splits,
+            "kernels": kernels,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e_leg(args, api, dw, wl, sharded, ws, err, stream, out, lse, tidx, tcnt, dev):
+    """The decode through the C ABI with host buffers (see run_product)."""
     import dataclasses
+
+    import torch
 
     from dsa_sparse_attention_decode_gb300.api import DecodeDesc
 
-    in_src = [dw.q_idx, dw.w_idx, dw.q, dw.rows.row_start, dw.rows.row_pos,
-              dw.idx_k.block_table, dw.kv.block_table]
+    R, H, k = wl.R, wl.H, wl.topk
+    ik = dw.idx_k_shards if sharded else [dw.idx_k]
+    kv = dw.kv_shards if sharded else [dw.kv]
+    W = len(ik)
+    in_src = [dw.q_idx, dw.w_idx, dw.q, dw.rows.row_start, dw.rows.row_pos]
+    bt_at = []
+    for c in list(ik) + list(kv):
+        if c.block_table is not None:
+            bt_at.append(len(in_src))
+            in_src.append(c.block_table)
+        else:
+            bt_at.append(None)
     offs, total = [], 0
     for t in in_src:
         offs.append(total)
@@ -538,13 +618,13 @@ def run_product(args):
             nb = t.numel() * t.element_size()
             views.append(dp[o:o + nb].view(t.dtype).view(t.shape))
         rows_e = dataclasses.replace(dw.rows, row_start=views[3], row_pos=views[4])
-        idx_e = dataclasses.replace(dw.idx_k, block_table=views[5])
-        kv_e = dataclasses.replace(dw.kv, block_table=views[6])
+        caches = [c if j is None else dataclasses.replace(c, block_table=views[j])
+                  for c, j in zip(list(ik) + list(kv), bt_at)]
         dr = torch.empty(o_elems + R * H, dtype=torch.float32, device=dev)
         d_pack.append(dp)
         d_res.append(dr)
         h_res.append(torch.empty(o_elems + R * H, dtype=torch.float32, pin_memory=True))
-        desc_e.append(DecodeDesc([idx_e], [kv_e], rows_e, views[0], views[1], views[2],
+        desc_e.append(DecodeDesc(caches[:W], caches[W:], rows_e, views[0], views[1], views[2],
                                  wl.sm_scale, k, dr[:o_elems].view(R, H, 512),
                                  dr[o_elems:].view(R, H), out_topk_idx=tidx, out_topk_count=tcnt))
     h2d = sum(t.numel() * t.element_size() for t in in_src)
@@ -588,62 +668,22 @@ def run_product(args):
     e2e_ms = e2e_run(args.steps)
     e2e_value, _, _ = aggregate(R * args.steps, e2e_ms / 1e3, device=dev)
     torch.cuda.synchronize()
+    if api.dsa_read_error(err) != 0:
+        raise SystemExit("device error word set in the end-to-end leg")
+    # the device leg's last full step left its O and LSE in `out` / `lse`
+    # (the per-kernel timing rewrote them with the same values)
     last = (args.steps - 1) & 1
     got = torch.from_numpy(h_res[last].numpy().copy())
     if not (torch.equal(got[:o_elems].view(R, H, 512), out.cpu())
             and torch.equal(got[o_elems:].view(R, H), lse.cpu())):
         raise SystemExit("the end-to-end leg and the device leg disagree")
-
-    # ---- roofline of the dominant kernel (the indexer: most of the bytes)
-    idx_bytes, mla_bytes = algorithmic_bytes(wl)
-    peaks, peak_kind = measured_peaks()
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    ach = idx_bytes / (kern_us["indexer"] * 1e-6) / 1e9
-    path_gbs = (idx_bytes + mla_bytes) / (ms_per_step * 1e-3) / 1e9
-    roofline = {"kernel": "indexer_kernel (dsa_indexer_scores)", "bound": "hbm",
-                "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(ach / hbm, 4), "peak_source": peak_kind,
-                "algorithmic_bytes_per_launch": idx_bytes,
-                "traffic": ncu_traffic("indexer"),
-                "path_algorithmic_bytes_per_step": idx_bytes + mla_bytes,
-                "path_achieved_gbs": round(path_gbs, 1),
-                "path_frac_of_measured": round(path_gbs / hbm, 4),
-                "path_frac_of_nominal_8tbs": round(path_gbs / NOMINAL_HBM_GBS, 4)}
-
-    # ---- CPU oracle baseline on a bounded sample (rank 0, N = 1 only)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, args.cpu_seconds)
-
-    if rank == 0:
-        launches_per_step = 3 + (1 if lay.num_parts > 1 else 0)
-        line = {
-            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded N(0,1)/N(0,0.5) bf16 caches and queries, U(0,1)/8 weights)",
-            "config": {"workload": WORKLOAD, "global_batch": R * world, "seq_len": 32768,
-                       "topk": k, "mla_heads": H, "num_splits": lay.num_splits,
-                       "l2": "flushed between timed steps (512 MB write, then 256 MB read); step stream ~350 MB > L2",
-                       "parallelism": f"dp{world} (independent request batches per GPU)"},
-            "roofline": roofline,
-            "kernels_us": {n: round(v, 2) for n, v in kern_us.items()},
-            "cpu_baseline": cpu,
-            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h,
-                    "note": "per-step inputs (queries, weights, rows, block tables) from pinned "
-                            "host memory and O/LSE back; caches stay resident in HBM; steps "
-                            "pipelined (input copy of step i+1 and result copy of step i-1 on "
-                            "two copy streams while step i computes, double-buffered device "
-                            "inputs/outputs), one timed region over all steps, no L2 flush "
-                            "inside it (each step streams ~350 MB > L2)"},
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clk.summary(),
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    return {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "note": "per-step inputs (queries, weights, rows, block tables) from pinned host "
+                    "memory and O/LSE back; caches stay resident in HBM; steps pipelined "
+                    "(input copy of step i+1 and result copy of step i-1 on two copy streams "
+                    "while step i computes, double-buffered device inputs/outputs), one timed "
+                    "region over all steps, no L2 flush inside it"}
 
 
 # ----------------------------------------------------------------- CPU oracle
@@ -654,17 +694,20 @@ def cpu_baseline(wl, seconds: float):
 
     rows, t0 = 0, time.perf_counter()
     r = 0
+    toks = 0
     while True:
         orc.decode_row(wl, r % wl.R)
+        toks += int(wl.row_pos[r % wl.R]) + 1
         rows += 1
         r += 1
         el = time.perf_counter() - t0
         if el >= seconds and rows >= 2:
             break
     return {"value": round(rows / el, 3), "unit": UNIT, "cores": _CORES, "kind": "oracle",
-            "sample": f"{rows} query rows of the same workload, one after another, full path "
-                      f"(indexer over 32768 tokens, exact top-2048, MLA) in float64 numpy, "
-                      f"{el:.1f} s"}
+            "sample": f"{rows} query rows of the same workload (rows 0..{min(rows, wl.R) - 1} in "
+                      f"order, {toks / rows:.0f} cached tokens per row on average), one after "
+                      f"another, full path (indexer over the row's tokens, exact "
+                      f"top-{wl.topk}, MLA) in float64 numpy, {el:.1f} s"}
 
 
 def run_reference(args):
@@ -672,9 +715,9 @@ def run_reference(args):
     if rank != 0:
         return
     from oracle import dsa_oracle as orc
-    from workloads import config_spec, make_workload
+    from workloads import make_workload
 
-    wl = make_workload(config_spec(1))
+    wl = make_workload(workload_spec(args))
     for i in range(args.warmup):
         orc.decode_row(wl, i % wl.R)
     t0 = time.perf_counter()
@@ -682,16 +725,19 @@ def run_reference(args):
         orc.decode_row(wl, i % wl.R)  # each step: one sampled row of the batch
     el = time.perf_counter() - t0
     value = args.steps / el
+    cfg = describe(wl)
+    cfg["parallelism"] = f"dp{args.gpus} (independent request batches per GPU)"
+    cfg["l2"] = "not applicable: the oracle runs on the host cores"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": 32, "seq_len": 32768,
-                   "parallelism": "host cores"},
+        "config": cfg,
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": _CORES,
                          "kind": "oracle",
-                         "sample": "one query row of the batch per step (full path, float64)"},
+                         "sample": "one query row of the batch per step, rows 0, 1, 2, ... "
+                                   "(full path, float64 numpy)"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -702,9 +748,6 @@ if __name__ == "__main__":
     a = parse()
     if a.kernel is not None:
         run_kernel_only(a)
-        sys.exit(0)
-    if a.config is not None:
-        run_config(a)
         sys.exit(0)
     if a.warmup < 3 and a.impl == "product":
         a.warmup = 3

@@ -59,3 +59,30 @@ def test_kernel_mode_is_parsed(monkeypatch):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--kernel", "topk", "--steps", "2", "--warmup", "1"])
     a = bench.parse()
     assert a.kernel == "topk" and a.steps == 2 and a.warmup == 1 and a.gpus == 1
+
+
+def test_default_workload_is_the_largest_configuration(monkeypatch):
+    """With no flags the contract line times the ragged fp8 sweep at B = 256;
+    --config selects another configuration."""
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse()
+    s = bench.workload_spec(a)
+    assert (s.B, s.dtype, s.length_law, s.L_lo, s.L_hi, s.topk, s.H) == (
+        256, "fp8_e4m3", "loguniform", 4096, 131072, 2048, 32)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--config", "1"])
+    s1 = bench.workload_spec(bench.parse())
+    assert (s1.B, s1.L, s1.dtype) == (32, 32768, "bf16")
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--config", "4", "--batch", "64"])
+    assert bench.workload_spec(bench.parse()).B == 64
+
+
+def test_algorithmic_bytes_closed_form():
+    """Per-kernel algorithmic bytes of a tiny bf16 workload, written out."""
+    from workloads import config_spec, make_workload
+
+    wl = make_workload(config_spec(1, B=2, L=300, H=16))
+    b = bench.algorithmic_bytes(wl)
+    L, k, H = 300, 2048, 16
+    assert b["indexer"] == 2 * (L * 256 + 5 * 4) + 2 * (64 * 128 * 2 + 64 * 4)
+    assert b["topk"] == 2 * (L * 4 + k * 4 + 4)
+    assert b["mla"] == 2 * (L * 1152 + k * 4 + H * 576 * 2 + H * 512 * 4 + H * 4)
