@@ -312,13 +312,15 @@ def run_kernel_only(args):
                          dtype=torch.uint8, device=dev)
     if args.kernel == "cache_write":
         return time_cache_write(args, dw, spec, dev, err)
+    topk_ws = torch.empty(max(1, api.dsa_topk_workspace_size(R, lay.ld_scores)), dtype=torch.uint8,
+                          device=dev)
     pre_ws = torch.empty(max(1, api.dsa_sparse_mla_prefill_into_workspace_size(R, H, k, 0)),
                          dtype=torch.uint8, device=dev)
     out_max = torch.empty(R, H, device=dev)
     fn = {
         "indexer": lambda: api.dsa_indexer_scores(dw.q_idx, dw.w_idx, dw.idx_k, dw.rows, scores,
                                                   err),
-        "topk": lambda: api.dsa_topk(scores, valid, k, tidx, tcnt, err),
+        "topk": lambda: api.dsa_topk(scores, valid, k, tidx, tcnt, err, workspace=topk_ws),
         "mla": lambda: api.dsa_sparse_mla_decode(dw.q, wl.sm_scale, dw.kv, dw.rows, tidx, tcnt,
                                                  out, lse, err, workspace=mla_ws,
                                                  num_splits=lay.num_splits),
@@ -491,8 +493,10 @@ def run_product(args):
         kern = {}
         kern["indexer"] = timed(lambda: api.dsa_indexer_scores(
             dw.q_idx, dw.w_idx, dw.idx_k, dw.rows, scores, err, stream=stream), args.steps)
+        topk_ws = torch.empty(max(1, api.dsa_topk_workspace_size(R, lay.ld_scores)),
+                              dtype=torch.uint8, device=dev)
         kern["topk"] = timed(lambda: api.dsa_topk(scores, valid, k, tidx, tcnt, err,
-                                                  stream=stream), args.steps)
+                                                  workspace=topk_ws, stream=stream), args.steps)
         mla_ws = torch.empty(max(1, api.dsa_sparse_mla_decode_workspace_size(
             R, H, k, lay.num_splits)), dtype=torch.uint8, device=dev)
         kern["mla"] = timed(lambda: api.dsa_sparse_mla_decode(

@@ -89,6 +89,7 @@ class DsaDecodeLayout(ctypes.Structure):
         ("cand_count", c_int64),
         ("topk_idx", c_int64),
         ("topk_count", c_int64),
+        ("topk_ws", c_int64),
         ("owned_local", c_int64),
         ("owned_count", c_int64),
         ("part_out", c_int64),
@@ -106,8 +107,9 @@ PROTOTYPES = {
     "dsa_read_error": (c_int, [c_void_p, POINTER(c_int32), c_void_p]),
     "dsa_indexer_scores": (c_int, [c_void_p, c_void_p, POINTER(DsaPagedCache), POINTER(DsaRows),
                                    c_int32, c_int32, c_void_p, c_int64, c_void_p, c_void_p]),
+    "dsa_topk_workspace_size": (c_size_t, [c_int32, c_int64]),
     "dsa_topk": (c_int, [c_void_p, c_int64, c_void_p, c_int32, c_int32, c_int32, c_int32,
-                         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+                         c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
     "dsa_shard_topk_merge": (c_int, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dsa_sparse_mla_decode_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32]),

@@ -105,11 +105,17 @@ def dsa_indexer_scores(q_idx, w_idx, idx_k: PagedCache, rows: Rows, scores, d_er
                                       _ptr(d_err), _stream(stream)), "dsa_indexer_scores")
 
 
+def dsa_topk_workspace_size(num_rows: int, ld_scores: int) -> int:
+    return int(C.lib().dsa_topk_workspace_size(num_rows, ld_scores))
+
+
 def dsa_topk(scores, valid_len, k: int, out_idx, out_count, d_err, out_score=None,
-             index_stride: int = 1, index_offset: int = 0, stream=None):
+             index_stride: int = 1, index_offset: int = 0, workspace=None, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(C.lib().dsa_topk(_ptr(scores), int(scores.shape[1]), _ptr(valid_len),
                             int(scores.shape[0]), k, index_stride, index_offset, _ptr(out_idx),
-                            _ptr(out_score), _ptr(out_count), _ptr(d_err), _stream(stream)),
+                            _ptr(out_score), _ptr(out_count), _ptr(workspace), ws_bytes,
+                            _ptr(d_err), _stream(stream)),
            "dsa_topk")
 
 

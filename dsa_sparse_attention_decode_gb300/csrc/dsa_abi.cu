@@ -273,15 +273,26 @@ int dsa_indexer_scores(const uint16_t* q_idx, const float* w_idx, const dsa_page
   return cuda_status(launch_indexer(L, static_cast<cudaStream_t>(stream)));
 }
 
+size_t dsa_topk_workspace_size(int32_t num_rows, int64_t ld_scores) {
+  if (num_rows <= 0 || ld_scores < 0 || ld_scores > INT32_MAX) return 0;
+  return topk_workspace_bytes(num_rows, ld_scores);
+}
+
 int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* valid_len, int32_t num_rows,
              int32_t k, int32_t index_stride, int32_t index_offset, int32_t* out_idx,
-             float* out_score, int32_t* out_count, int32_t* d_err, void* stream) {
+             float* out_score, int32_t* out_count, void* workspace, size_t workspace_bytes,
+             int32_t* d_err, void* stream) {
   if (num_rows < 0 || k < 1 || k > 4096 || d_err == nullptr || ld_scores < 0)
     return DSA_ERR_INVALID_ARG;
   if (num_rows == 0) return DSA_OK;
   if (scores == nullptr || valid_len == nullptr || out_idx == nullptr || out_count == nullptr)
     return DSA_ERR_INVALID_ARG;
   if (ld_scores > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+  if (workspace != nullptr) {
+    if (workspace_bytes < topk_workspace_bytes(num_rows, ld_scores))
+      return DSA_ERR_WORKSPACE_TOO_SMALL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return DSA_ERR_INVALID_ARG;
+  }
   TopkLaunch L{};
   L.scores = scores;
   L.ld = ld_scores;
@@ -300,7 +311,12 @@ int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* valid_len, i
   L.out_score = out_score;
   L.out_count = out_count;
   L.d_err = d_err;
-  return cuda_status(launch_topk(L, static_cast<cudaStream_t>(stream)));
+  topk_set_workspace(L, workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (workspace != nullptr && topk_uses_workspace(num_rows, ld_scores) &&
+      cudaMemsetAsync(workspace, 0, topk_workspace_clear_bytes(num_rows), s) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  return cuda_status(launch_topk(L, s));
 }
 
 int dsa_shard_topk_merge(const float* cand_score, const int32_t* cand_pos,
@@ -465,6 +481,7 @@ int dsa_decode_workspace_layout(const dsa_decode_desc* d, dsa_decode_layout* lay
   }
   L.topk_idx = d->out_topk_idx ? -1 : take(R * k * 4);
   L.topk_count = d->out_topk_count ? -1 : take(R * 4);
+  L.topk_ws = take(static_cast<int64_t>(topk_workspace_bytes(static_cast<int>(W * R), L.ld_scores)));
   const int64_t expected = (k < d->rows.max_len ? k : d->rows.max_len) / W;
   const int S = resolve_splits(d->num_splits, static_cast<int>(W * R), static_cast<int>(k),
                                static_cast<int>(expected > 0 ? expected : 1));
@@ -509,6 +526,10 @@ int dsa_decode(const dsa_decode_desc* d, void* workspace, size_t workspace_bytes
   // before them: each starts launching while its predecessor runs and waits
   // for it before touching the predecessor's outputs.  The indexer follows
   // the caller's work and is launched plainly.
+  // 0. the top-k histograms and candidate counts start at zero
+  if (topk_uses_workspace(W * R, lay.ld_scores) &&
+      cudaMemsetAsync(ws + lay.topk_ws, 0, topk_workspace_clear_bytes(W * R), s) != cudaSuccess)
+    return DSA_ERR_CUDA;
   // 1. indexer over every shard's cache, one launch
   {
     IndexerLaunch L{};
@@ -564,6 +585,7 @@ int dsa_decode(const dsa_decode_desc* d, void* workspace, size_t workspace_bytes
       L.out_count = topk_cnt;
     }
     L.d_err = d_err;
+    topk_set_workspace(L, ws + lay.topk_ws);
     if (launch_topk(L, s, true) != cudaSuccess) return DSA_ERR_CUDA;
   }
   // 3. exact merge of the shards' candidates; owned local rows per shard

@@ -63,10 +63,28 @@ struct TopkLaunch {
   float* out_score;           // or NULL
   int32_t* out_count;
   int32_t* d_err;
+  // workspace of the segment-parallel form (all NULL: one CTA per row does
+  // every pass); set by topk_set_workspace
+  uint32_t* ghist;            // [rows][1024] first histograms (zeroed before the launch)
+  uint32_t* gcnt;             // [rows] candidates listed (zeroed before the launch)
+  uint2* gcand;               // [rows][4096] candidates (key, position)
+  uint32_t* gbits;            // [rows][nw] position bitmaps of the keys above the range
+  int32_t nw;                 // bitmap words per row
+  int32_t seg_quads;          // positions / 4 per segment CTA (set by the launcher)
 };
 // pdl: launch as a programmatic dependent of the stream's previous kernel (only
-// after kernels of this library whose outputs the kernel waits for)
+// after kernels of this library whose outputs the kernel waits for).  With a
+// workspace, its first topk_workspace_clear_bytes() bytes must be zero when
+// the launch starts (the caller clears them on the stream beforehand).
 cudaError_t launch_topk(const TopkLaunch& p, cudaStream_t stream, bool pdl = false);
+// workspace bytes of the segment-parallel form for `rows` score rows of stride ld
+size_t topk_workspace_bytes(int rows, int64_t ld);
+size_t topk_workspace_clear_bytes(int rows);
+// whether launch_topk uses a workspace for these sizes (else it ignores it)
+bool topk_uses_workspace(int rows, int64_t ld);
+// point p's workspace fields into ws (NULL: the one-CTA-per-row form); needs
+// p.nshards, p.rows and p.ld
+void topk_set_workspace(TopkLaunch& p, void* ws);
 
 // ------------------------------------------------------------- shard merge
 

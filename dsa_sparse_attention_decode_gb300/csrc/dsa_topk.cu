@@ -24,7 +24,10 @@
 //      ascending order: from the per-warp counts every warp knows its first
 //      output slot, and writes 128 keys' selections per step (4 per lane,
 //      warp scans for the slots).
-// No sort: the list comes out in position order.
+// No sort: the list comes out in position order.  This cluster form serves
+// launches of few rows (at most half the SM count: every row then gets a
+// cluster of 2 or 4 CTAs at once) and score rows too long for the position
+// bitmaps of the segment form below.
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
 #include "dsa_select.cuh"
@@ -723,6 +726,562 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(kThreads, 1)
   if constexpr (C > 1) cluster_sync();  // no CTA leaves while another may still read its smem
 }
 
+// ======================================================================
+// Segment-parallel selection with position bitmaps.
+//
+// Three kernels, so that every SM takes part in the passes over the scores
+// whatever the number and the lengths of the rows:
+//   K1 (one CTA per 16K-position segment of a row): a 1024-bin histogram of
+//      the segment's keys over a key window drawn from a sample of the row
+//      (keys below it count in bin 0, keys above it in the last bin), added
+//      to the row's histogram in the workspace;
+//   K2 (the same segments): the row's histogram gives the key range (bin)
+//      holding the k-th largest key; the segment's keys above the range are
+//      written as bits of the row's position bitmap (32 positions per word),
+//      and the keys inside it are listed as candidates (key, position);
+//   K3 (one 512-thread CTA per row): the threshold key T comes from 10-bit
+//      histogram rounds over the candidates alone; candidates above T join
+//      the bitmap and those equal to T go to a bitmap of ties; compaction
+//      walks the bitmap words in position order, takes ties lowest positions
+//      first (as many as the selection still needs), and prefix sums over
+//      the threads give every selected position its output slot.  The list
+//      comes out in ascending position order without a sort.
+// A row whose threshold bin holds more keys than the candidate list takes
+// (only rows with massive ties or a degenerate spread) is resolved by K3
+// alone with further 4096-bin rounds over the row.  Without a workspace K3
+// runs alone and makes its own histogram and bitmap pass.
+// A window that follows the row's own spread keeps neighbouring keys in
+// different bins: fixed top key bits would put a row of scores within one
+// octave into a few bins, whose shared-memory atomics serialize.
+constexpr int kRThreads = 512;      // K3
+constexpr int kSThreads = 256;      // K1, K2
+constexpr int kWBits = 10;          // first histogram: 1024 bins over the sampled window
+constexpr int kWBins = 1 << kWBits;
+constexpr int kRBits = 12;          // further rounds over a row: 4096 bins
+constexpr int kRCand = 4096;        // candidate list capacity
+constexpr int kCBits = 10;          // rounds over the candidates
+constexpr int kSample = 512;        // sampled positions of a row
+constexpr int kRMisc = 256;         // words: [0, 32) scalars, [32, 128) scratch
+constexpr int kU = 6;               // quads in flight per thread and step
+
+struct RowsSmem {
+  int nw;  // bitmap words (covers ld positions, a multiple of 4)
+  int off_hist, off_cand, off_eq, off_gt, off_chist, off_misc, total;
+};
+
+__host__ inline RowsSmem rows_smem(int64_t ld) {
+  RowsSmem s{};
+  s.nw = static_cast<int>(((ld + 31) / 32 + 3) / 4 * 4);
+  const int a_hist = (1 << kRBits) * 4;
+  const int a_cand = kRCand * 8 + s.nw * 4;  // the candidates and the tie bitmap
+  // the histogram is dead before the candidate list and the tie bitmap are written
+  const int a = a_hist > a_cand ? a_hist : a_cand;
+  s.off_hist = 0;
+  s.off_cand = 0;
+  s.off_eq = kRCand * 8;
+  s.off_gt = a;
+  s.off_chist = s.off_gt + s.nw * 4;
+  s.off_misc = s.off_chist + (1 << kCBits) * 4;
+  s.total = s.off_misc + kRMisc * 4;
+  return s;
+}
+
+// Exclusive prefix sum of v over the CTA's NT threads; *total gets the sum.
+// Uses scratch[0, NT / 32); every thread calls it.
+template <int NT>
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* scratch,
+                                                    uint32_t* total) {
+  constexpr int kW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t incl = warp_incl_scan(v, lane);
+  __syncthreads();  // scratch is free (an earlier call may still be reading it)
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  const uint32_t wt = lane < kW ? scratch[lane] : 0u;
+  const uint32_t winc = warp_incl_scan(wt, lane);
+  const uint32_t wex = __shfl_sync(0xffffffffu, winc - wt, warp);
+  *total = __shfl_sync(0xffffffffu, winc, kW - 1);
+  return wex + incl - v;
+}
+
+// The bin of hist[0, nb) (nb a power of two, 2 .. 4096; a higher bin holds
+// larger keys) that holds the k_rem-th largest key: (bin, k_rem within the
+// bin, the bin's count) to out[0..2].  Every thread calls it; the caller's
+// __syncthreads publishes the answer.
+template <int NT>
+__device__ void block_find_bin(const uint32_t* hist, int nb, uint32_t k_rem, uint32_t* out,
+                               uint32_t* scratch) {
+  const int tid = threadIdx.x;
+  const int per = nb >= NT ? nb / NT : 1;
+  const int b0 = tid * per;
+  uint32_t mine = 0;
+  if (b0 < nb) {
+    if (per >= 4) {
+      for (int j = 0; j < per; j += 4) {
+        const uint4 x = *reinterpret_cast<const uint4*>(hist + b0 + j);
+        mine += x.x + x.y + x.z + x.w;
+      }
+    } else {
+      for (int j = 0; j < per; ++j) mine += hist[b0 + j];
+    }
+  }
+  // keys in the bins of the threads above this one = total - inclusive prefix
+  uint32_t total;
+  const uint32_t ex = block_excl_scan<NT>(mine, scratch, &total);
+  const uint32_t above = total - ex - mine;
+  if (b0 < nb && above < k_rem && above + mine >= k_rem) {
+    uint32_t acc = above;
+    for (int j = per - 1; j >= 0; --j) {
+      const uint32_t h = hist[b0 + j];
+      if (acc + h >= k_rem) {
+        out[0] = static_cast<uint32_t>(b0 + j);
+        out[1] = k_rem - acc;
+        out[2] = h;
+        break;
+      }
+      acc += h;
+    }
+  }
+}
+
+// Bins of a key range [rlo, rhi] (inclusive): bin(key) = (key - rlo) >>
+// shift, with shift the bits of (rhi - rlo) beyond nbits, so that the range
+// splits into at most 2^nbits bins of 2^shift keys.
+__device__ __forceinline__ int range_shift(uint32_t rlo, uint32_t rhi, int nbits) {
+  const uint32_t wdt = rhi - rlo;
+  const int len = wdt == 0u ? 0 : 32 - __clz(wdt);
+  return len > nbits ? len - nbits : 0;
+}
+// the keys of bin b of [rlo, rhi] (the last bin may be short)
+__device__ __forceinline__ void bin_range(uint32_t rlo, uint32_t rhi, int shift, uint32_t b,
+                                          uint32_t* blo, uint32_t* bhi) {
+  const uint64_t l = static_cast<uint64_t>(rlo) + (static_cast<uint64_t>(b) << shift);
+  const uint64_t h = l + (1ull << shift) - 1ull;
+  *blo = static_cast<uint32_t>(l);
+  *bhi = h < rhi ? static_cast<uint32_t>(h) : rhi;
+}
+
+// A score row: its valid count and where it lives.
+struct RowRef {
+  const float* src;
+  int n;
+  int nq;    // quads of positions, (n + 3) / 4
+  bool vec;  // float4 loads: 16-byte aligned row start and stride a multiple of 4
+};
+
+__device__ __forceinline__ RowRef row_ref(const TopkLaunch& P, int q) {
+  const int w = q / P.rows;
+  const int r = q - w * P.rows;
+  RowRef R;
+  int n = P.valid_len ? P.valid_len[q] : shard_valid_len(P.row_pos[r], P.W, w + P.shard_offset);
+  n = n < 0 ? 0 : (n > P.ld ? static_cast<int>(P.ld) : n);
+  R.n = n;
+  R.nq = (n + 3) >> 2;
+  R.src = P.scores + static_cast<long long>(w) * P.shard_stride + static_cast<long long>(r) * P.ld;
+  R.vec = (reinterpret_cast<uintptr_t>(R.src) & 15u) == 0 && (P.ld & 3) == 0;
+  return R;
+}
+
+// The keys of quad qd (positions 4qd .. 4qd + 3); returns the valid mask.
+// With float4 loads every quad with 4qd < n lies inside the row's storage.
+__device__ __forceinline__ uint32_t load_quad(const RowRef& R, int qd, uint32_t* kv) {
+  if (qd >= R.nq) return 0u;
+  const int p = qd * 4;
+  float f[4];
+  if (R.vec) {
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(R.src + p));
+    f[0] = x.x;
+    f[1] = x.y;
+    f[2] = x.z;
+    f[3] = x.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) f[e] = p + e < R.n ? __ldcg(R.src + p + e) : 0.0f;
+  }
+  uint32_t ok = 0u;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    kv[e] = score_key(f[e]);
+    ok |= (p + e < R.n ? 1u : 0u) << e;
+  }
+  return ok;
+}
+
+// The row's key window: the smallest and the largest key of kSample evenly
+// spread positions (the same positions in every kernel) -> win[0], win[1].
+// Every thread calls it (n >= 1).
+template <int NT>
+__device__ void sample_window(const RowRef& R, uint32_t* scratch, uint32_t* win) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  for (int i = threadIdx.x; i < kSample; i += NT) {
+    const int p = static_cast<int>((static_cast<long long>(i) * R.n) / kSample);
+    const uint32_t key = score_key(__ldcg(R.src + p));
+    mn = min(mn, key);
+    mx = max(mx, key);
+  }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  __syncthreads();  // scratch is free
+  if (lane == 0) {
+    scratch[warp] = mn;
+    scratch[32 + warp] = mx;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t a = __reduce_min_sync(0xffffffffu, lane < NT / 32 ? scratch[lane] : 0xFFFFFFFFu);
+    const uint32_t b = __reduce_max_sync(0xffffffffu, lane < NT / 32 ? scratch[32 + lane] : 0u);
+    if (lane == 0) {
+      win[0] = a;
+      win[1] = b;
+    }
+  }
+  __syncthreads();
+}
+
+// bin of a key in the first histogram (window [wlo, ...] split 2^wshift wide)
+__device__ __forceinline__ uint32_t window_bin(uint32_t key, uint32_t wlo, int wshift) {
+  return key < wlo ? 0u : min(static_cast<uint32_t>(kWBins - 1), (key - wlo) >> wshift);
+}
+// the keys of first-histogram bin b (bin 0 reaches down to 0, the last bin up to ~0)
+__device__ __forceinline__ void window_range(uint32_t wlo, int wshift, uint32_t b, uint32_t* rlo,
+                                             uint32_t* rhi) {
+  bin_range(wlo, 0xFFFFFFFFu, wshift, b, rlo, rhi);
+  if (b == 0u) *rlo = 0u;
+  if (b == static_cast<uint32_t>(kWBins - 1)) *rhi = 0xFFFFFFFFu;
+}
+
+// First histogram over quads [q0, q1) of the row; returns whether a NaN was seen.
+template <int NT>
+__device__ bool window_hist_pass(const RowRef& R, int q0, int q1, uint32_t wlo, int wshift,
+                                 uint32_t* hist) {
+  bool nan_seen = false;
+  for (int base = q0; base < q1; base += NT * kU) {
+    uint32_t kv[kU][4], ok[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int qd = base + u * NT + static_cast<int>(threadIdx.x);
+      ok[u] = qd < q1 ? load_quad(R, qd, kv[u]) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if ((ok[u] >> e) & 1u) {
+          const uint32_t key = kv[u][e];
+          // NaN keys: above 0xFF800000 (+inf) or below 0x007FFFFF (-inf)
+          nan_seen |= key > 0xFF800000u || key < 0x007FFFFFu;
+          atomicAdd(hist + window_bin(key, wlo, wshift), 1u);
+        }
+  }
+  return nan_seen;
+}
+
+// Marking pass over the runs [r0, r1) of 32 quads (128 positions) of the
+// row: keys above rhi become bits of gt_out (word = position / 32); keys in
+// [rlo, rhi] become bits of eq_out when `exact`, else candidates appended at
+// cand_out[atomicAdd(cand_cnt)] (at most kRCand kept).  Lane l holds
+// positions 4l .. 4l + 3 of a run, so the word of positions 32j .. 32j + 31
+// is the OR of the 4-bit masks of lanes 8j .. 8j + 7.
+template <int NT>
+__device__ void mark_pass(const RowRef& R, int r0, int r1, uint32_t rlo, uint32_t rhi, bool exact,
+                          uint32_t* gt_out, uint32_t* eq_out, uint32_t* cand_cnt, uint2* cand_out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwu = (R.n + 31) >> 5;
+  for (int s0 = r0 + warp * kU; s0 < r1; s0 += (NT / 32) * kU) {
+    uint32_t kv[kU][4], ok[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) ok[u] = s0 + u < r1 ? load_quad(R, (s0 + u) * 32 + lane, kv[u]) : 0u;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (s0 + u >= r1) break;  // warp-uniform
+      uint32_t gn = 0u, en = 0u;  // 4-bit masks: above / inside the range
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool v = (ok[u] >> e) & 1u;
+        const uint32_t key = kv[u][e];
+        gn |= (v && key > rhi ? 1u : 0u) << e;
+        en |= (v && key >= rlo && key <= rhi ? 1u : 0u) << e;
+      }
+      const int sh4 = 4 * (lane & 7);
+      uint32_t gw = gn << sh4, ew = en << sh4;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) {
+        gw |= __shfl_xor_sync(0xffffffffu, gw, o);
+        ew |= __shfl_xor_sync(0xffffffffu, ew, o);
+      }
+      const int word = (s0 + u) * 4 + (lane >> 3);
+      if ((lane & 7) == 0 && word < nwu) {
+        gt_out[word] = gw;
+        if (exact) eq_out[word] = ew;
+      }
+      if (!exact && __any_sync(0xffffffffu, en != 0u)) {
+        const uint32_t c = __popc(en);
+        const uint32_t incl = warp_incl_scan(c, lane);
+        uint32_t slot = 0;
+        if (lane == 31) slot = atomicAdd(cand_cnt, incl);
+        slot = __shfl_sync(0xffffffffu, slot, 31) + incl - c;
+        const int p0 = ((s0 + u) * 32 + lane) * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if ((en >> e) & 1u) {
+            if (slot < static_cast<uint32_t>(kRCand))
+              cand_out[slot] = make_uint2(kv[u][e], static_cast<uint32_t>(p0 + e));
+            ++slot;
+          }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- K1
+__global__ void __launch_bounds__(kSThreads) topk_hist_kernel(const TopkLaunch P) {
+  __shared__ __align__(16) uint32_t hist[kWBins];
+  __shared__ uint32_t misc[128];
+  const int q = blockIdx.y;
+  pdl_trigger();
+  pdl_wait();  // the scores come from the previous grid
+  const RowRef R = row_ref(P, q);
+  const int q0 = blockIdx.x * P.seg_quads;
+  if (R.n <= P.k || q0 >= R.nq) return;
+  const int q1 = min(R.nq, q0 + P.seg_quads);
+  for (int i = threadIdx.x; i < kWBins; i += kSThreads) hist[i] = 0u;
+  sample_window<kSThreads>(R, misc + 32, misc);  // its barriers also publish the zeroed bins
+  const uint32_t wlo = misc[0];
+  const int wshift = range_shift(wlo, misc[1], kWBits);
+  const bool nan_seen = window_hist_pass<kSThreads>(R, q0, q1, wlo, wshift, hist);
+  if (__any_sync(0xffffffffu, nan_seen) && (threadIdx.x & 31) == 0) raise_err(P.d_err, DSA_DEVERR_NAN);
+  __syncthreads();
+  uint32_t* g = P.ghist + static_cast<long long>(q) * kWBins;
+  for (int i = threadIdx.x; i < kWBins; i += kSThreads)
+    if (hist[i] != 0u) atomicAdd(g + i, hist[i]);
+}
+
+// ---------------------------------------------------------------- K2
+__global__ void __launch_bounds__(kSThreads) topk_mark_kernel(const TopkLaunch P) {
+  __shared__ __align__(16) uint32_t hist[kWBins];
+  __shared__ uint32_t misc[128];
+  const int q = blockIdx.y;
+  pdl_trigger();
+  pdl_wait();  // the row histograms come from the previous grid
+  const RowRef R = row_ref(P, q);
+  const int q0 = blockIdx.x * P.seg_quads;
+  if (R.n <= P.k || q0 >= R.nq) return;
+  const int q1 = min(R.nq, q0 + P.seg_quads);
+  const uint32_t* g = P.ghist + static_cast<long long>(q) * kWBins;
+  for (int i = threadIdx.x; i < kWBins; i += kSThreads) hist[i] = __ldcg(g + i);
+  sample_window<kSThreads>(R, misc + 32, misc);
+  const uint32_t wlo = misc[0];
+  const int wshift = range_shift(wlo, misc[1], kWBits);
+  block_find_bin<kSThreads>(hist, kWBins, static_cast<uint32_t>(P.k), misc + 4, misc + 32);
+  __syncthreads();
+  if (misc[6] > static_cast<uint32_t>(kRCand)) return;  // crowded: K3 resolves the row alone
+  uint32_t rlo, rhi;
+  window_range(wlo, wshift, misc[4], &rlo, &rhi);
+  mark_pass<kSThreads>(R, q0 / 32, (q1 + 31) / 32, rlo, rhi, false,
+                       P.gbits + static_cast<long long>(q) * P.nw, nullptr, P.gcnt + q,
+                       P.gcand + static_cast<long long>(q) * kRCand);
+}
+
+// ---------------------------------------------------------------- K3
+__global__ void __launch_bounds__(kRThreads, 2) topk_rows_kernel(const TopkLaunch P,
+                                                              const RowsSmem S) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + S.off_hist);
+  uint2* cand = reinterpret_cast<uint2*>(smem + S.off_cand);
+  uint32_t* eqb = reinterpret_cast<uint32_t*>(smem + S.off_eq);
+  uint32_t* gtb = reinterpret_cast<uint32_t*>(smem + S.off_gt);
+  uint32_t* chist = reinterpret_cast<uint32_t*>(smem + S.off_chist);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + S.off_misc);
+  uint32_t* sh = misc;            // [0] NaN seen, [1] candidates, [4..6] bin search, [8..9] window
+  uint32_t* scratch = misc + 32;  // [96] scan and reduction scratch
+
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int q = blockIdx.x;
+  const int w = q / P.rows;
+  const int r = q - w * P.rows;
+  const int k = P.k;
+  pdl_trigger();
+  pdl_wait();  // the scores (or the marks of K2) come from the previous grid
+
+  {
+    const int nraw = P.valid_len ? P.valid_len[q]
+                                 : shard_valid_len(P.row_pos[r], P.W, w + P.shard_offset);
+    if ((nraw < 0 || nraw > P.ld) && tid == 0) raise_err(P.d_err, DSA_DEVERR_INDEX);
+  }
+  const RowRef R = row_ref(P, q);
+  const int n = R.n;
+  const int off = P.index_offset + (P.offset_per_shard ? (w + P.shard_offset) : 0);
+  int32_t* oi = P.out_idx + static_cast<long long>(q) * k;
+  float* os = P.out_score ? P.out_score + static_cast<long long>(q) * k : nullptr;
+  const int cnt_all = n < k ? n : k;
+  if (tid < 32) sh[tid] = 0;
+
+  if (n <= k) {
+    // every valid position, in order
+    bool nan_seen = false;
+    for (int i = tid; i < n; i += kRThreads) {
+      const float f = __ldcg(R.src + i);
+      nan_seen |= (f != f);
+      oi[i] = i * P.index_stride + off;
+      if (os) os[i] = f;
+    }
+    for (int i = n + tid; i < k; i += kRThreads) {
+      oi[i] = -1;
+      if (os) os[i] = -__int_as_float(0x7f800000);
+    }
+    if (tid == 0) P.out_count[q] = cnt_all;
+    if (__any_sync(0xffffffffu, nan_seen) && lane == 0) raise_err(P.d_err, DSA_DEVERR_NAN);
+    return;
+  }
+
+  // ---------------- the first histogram: K1's, or made here
+  if (P.ghist != nullptr) {
+    const uint32_t* g = P.ghist + static_cast<long long>(q) * kWBins;
+    for (int i = tid; i < kWBins; i += kRThreads) hist[i] = __ldcg(g + i);
+  } else {
+    for (int i = tid; i < kWBins; i += kRThreads) hist[i] = 0u;
+  }
+  sample_window<kRThreads>(R, scratch, sh + 8);  // its barriers publish the bins and sh
+  const uint32_t wlo = sh[8];
+  const int wshift = range_shift(wlo, sh[9], kWBits);
+  if (P.ghist == nullptr) {
+    const bool nan_seen = window_hist_pass<kRThreads>(R, 0, R.nq, wlo, wshift, hist);
+    if (__any_sync(0xffffffffu, nan_seen) && lane == 0) raise_err(P.d_err, DSA_DEVERR_NAN);
+    __syncthreads();
+  }
+  block_find_bin<kRThreads>(hist, kWBins, static_cast<uint32_t>(k), sh + 4, scratch);
+  __syncthreads();
+  // [rlo, rhi]: the keys of the bin holding T; k_rem: T's rank in it from the
+  // top; cnt: the row's keys in it
+  uint32_t rlo, rhi, k_rem = sh[5], cnt = sh[6];
+  window_range(wlo, wshift, sh[4], &rlo, &rhi);
+  const int nwu = (n + 31) >> 5;  // bitmap words in use
+  bool exact = false;
+  uint32_t nc;
+  if (P.ghist != nullptr && cnt <= static_cast<uint32_t>(kRCand)) {
+    // ---------------- K2's bitmap and candidates
+    __syncthreads();  // the histogram is dead: its memory holds the candidates next
+    const uint32_t* gb = P.gbits + static_cast<long long>(q) * P.nw;
+    for (int j = tid; j < S.nw; j += kRThreads) {
+      gtb[j] = j < nwu ? __ldcg(gb + j) : 0u;
+      eqb[j] = 0u;
+    }
+    nc = min(__ldcg(P.gcnt + q), static_cast<uint32_t>(kRCand));
+    const uint2* gc = P.gcand + static_cast<long long>(q) * kRCand;
+    for (uint32_t e = tid; e < nc; e += kRThreads) cand[e] = __ldcg(gc + e);
+    __syncthreads();
+  } else {
+    // ---------------- further rounds while the bin is crowded
+    while (cnt > static_cast<uint32_t>(kRCand) && rlo < rhi) {
+      const int shift = range_shift(rlo, rhi, kRBits);
+      __syncthreads();  // every thread has read sh and the previous histogram
+      for (int i = tid; i < (1 << kRBits); i += kRThreads) hist[i] = 0u;
+      __syncthreads();
+      for (int base = 0; base < R.nq; base += kRThreads * kU) {
+        uint32_t kv[kU][4], ok[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) ok[u] = load_quad(R, base + u * kRThreads + tid, kv[u]);
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t key = kv[u][e];
+            if (((ok[u] >> e) & 1u) && key >= rlo && key <= rhi)
+              atomicAdd(hist + ((key - rlo) >> shift), 1u);
+          }
+      }
+      __syncthreads();
+      block_find_bin<kRThreads>(hist, 1 << kRBits, k_rem, sh + 4, scratch);
+      __syncthreads();
+      bin_range(rlo, rhi, shift, sh[4], &rlo, &rhi);
+      k_rem = sh[5];
+      cnt = sh[6];
+    }
+    exact = rlo == rhi;  // T is known: every key in the range equals it
+    __syncthreads();     // the histogram is dead: its memory holds the candidates next
+    for (int j = tid; j < S.nw; j += kRThreads) {
+      gtb[j] = 0u;
+      eqb[j] = 0u;
+    }
+    __syncthreads();
+    mark_pass<kRThreads>(R, 0, (R.nq + 31) / 32, rlo, rhi, exact, gtb, eqb, sh + 1, cand);
+    __syncthreads();
+    nc = min(sh[1], static_cast<uint32_t>(kRCand));
+  }
+
+  // ---------------- T from the candidates alone (10-bit rounds over the range)
+  if (!exact) {
+    while (rlo < rhi) {
+      const int shift = range_shift(rlo, rhi, kCBits);
+      for (int i = tid; i < (1 << kCBits); i += kRThreads) chist[i] = 0u;
+      __syncthreads();
+      for (uint32_t e = tid; e < nc; e += kRThreads) {
+        const uint32_t key = cand[e].x;
+        if (key >= rlo && key <= rhi) atomicAdd(chist + ((key - rlo) >> shift), 1u);
+      }
+      __syncthreads();
+      block_find_bin<kRThreads>(chist, 1 << kCBits, k_rem, sh + 4, scratch);
+      __syncthreads();
+      bin_range(rlo, rhi, shift, sh[4], &rlo, &rhi);
+      k_rem = sh[5];
+      __syncthreads();  // sh and chist are read before the next round writes them
+    }
+    // candidates above T are selected; those equal to T are ties
+    for (uint32_t e = tid; e < nc; e += kRThreads) {
+      const uint2 c = cand[e];
+      if (c.x > rlo) atomicOr(gtb + (c.y >> 5), 1u << (c.y & 31u));
+      else if (c.x == rlo) atomicOr(eqb + (c.y >> 5), 1u << (c.y & 31u));
+    }
+    __syncthreads();
+  }
+  // k_rem: ties (keys equal to T) to take, lowest positions first
+
+  // ---------------- compaction in position order
+  const int per = (nwu + kRThreads - 1) / kRThreads;
+  const int j0 = tid * per, j1 = min(nwu, j0 + per);
+  uint32_t e_mine = 0;
+  for (int j = j0; j < j1; ++j) e_mine += __popc(eqb[j]);
+  uint32_t e_tot;
+  uint32_t eq_before = block_excl_scan<kRThreads>(e_mine, scratch, &e_tot);
+  uint32_t s_mine = 0;
+  for (int j = j0; j < j1; ++j) {
+    uint32_t ew = eqb[j];
+    const uint32_t room = eq_before < k_rem ? k_rem - eq_before : 0u;
+    const uint32_t pe = __popc(ew);
+    if (pe > room) {  // keep the lowest `room` ties of the word
+      uint32_t keep = 0u;
+      for (uint32_t t = 0; t < room; ++t) {
+        const uint32_t bit = ew & (0u - ew);
+        keep |= bit;
+        ew ^= bit;
+      }
+      ew = keep;
+    }
+    eq_before += pe;
+    eqb[j] = ew;  // this thread's words only
+    s_mine += __popc(gtb[j] | ew);
+  }
+  uint32_t s_tot;
+  uint32_t slot = block_excl_scan<kRThreads>(s_mine, scratch, &s_tot);
+  for (int j = j0; j < j1 && slot < static_cast<uint32_t>(k); ++j) {
+    uint32_t sel = gtb[j] | eqb[j];
+    while (sel != 0u && slot < static_cast<uint32_t>(k)) {
+      const int b = __ffs(sel) - 1;
+      sel &= sel - 1u;
+      const int pos = j * 32 + b;
+      oi[slot] = pos * P.index_stride + off;
+      if (os) os[slot] = key_score(score_key(__ldcg(R.src + pos)));  // -0 listed as +0
+      ++slot;
+    }
+  }
+  for (int i = cnt_all + tid; i < k; i += kRThreads) {
+    oi[i] = -1;
+    if (os) os[i] = -__int_as_float(0x7f800000);
+  }
+  if (tid == 0) P.out_count[q] = cnt_all;
+}
+
 template <int C>
 cudaError_t launch_c(const TopkLaunch& p, int rows, cudaStream_t stream, bool pdl) {
   const TopkSmem S = topk_smem(C);
@@ -734,14 +1293,77 @@ cudaError_t launch_c(const TopkLaunch& p, int rows, cudaStream_t stream, bool pd
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkLaunch& p, cudaStream_t stream, bool pdl) {
-  const int rows = p.nshards * p.rows;
-  if (rows == 0) return cudaSuccess;
-  // the widest cluster that still runs every row at once (one CTA per SM)
+size_t topk_workspace_bytes(int rows, int64_t ld) {
+  if (rows <= 0) return 0;
+  const int64_t nw = ((ld + 31) / 32 + 3) / 4 * 4;
+  const int64_t R = rows;
+  const int64_t hist = R * kWBins * 4 + (R * 4 + 255) / 256 * 256;  // histograms, counts
+  return static_cast<size_t>(hist + R * kRCand * 8 + R * nw * 4);
+}
+
+void topk_set_workspace(TopkLaunch& p, void* ws) {
+  const int64_t R = static_cast<int64_t>(p.nshards) * p.rows;
+  p.nw = static_cast<int32_t>(((p.ld + 31) / 32 + 3) / 4 * 4);
+  if (ws == nullptr || R == 0) {
+    p.ghist = p.gcnt = p.gbits = nullptr;
+    p.gcand = nullptr;
+    return;
+  }
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  p.ghist = reinterpret_cast<uint32_t*>(b);
+  p.gcnt = reinterpret_cast<uint32_t*>(b + R * kWBins * 4);
+  b += R * kWBins * 4 + (R * 4 + 255) / 256 * 256;
+  p.gcand = reinterpret_cast<uint2*>(b);
+  b += R * kRCand * 8;
+  p.gbits = reinterpret_cast<uint32_t*>(b);
+}
+
+size_t topk_workspace_clear_bytes(int rows) {
+  const int64_t R = rows;
+  return static_cast<size_t>(R * kWBins * 4 + R * 4);
+}
+
+bool topk_uses_workspace(int rows, int64_t ld) {
   const int sms = num_sms() > 0 ? num_sms() : 148;
-  if (rows * 4 <= sms) return launch_c<4>(p, rows, stream, pdl);
-  if (rows * 2 <= sms) return launch_c<2>(p, rows, stream, pdl);
-  return launch_c<1>(p, rows, stream, pdl);
+  return rows > 0 && rows <= 65535 && rows * 2 > sms && rows_smem(ld).total <= kSmemLimit;
+}
+
+cudaError_t launch_topk(const TopkLaunch& p0, cudaStream_t stream, bool pdl) {
+  const int rows = p0.nshards * p0.rows;
+  if (rows == 0) return cudaSuccess;
+  TopkLaunch p = p0;
+  const RowsSmem RS = rows_smem(p.ld);
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  // Few rows (every row gets a cluster of 2 or 4 CTAs at once) or rows too
+  // long for the bitmaps: the cluster form, the widest cluster that still
+  // runs every row at once (one CTA per SM).  Measured on one GB300: 32 rows
+  // of 32768 scores in 18.4 us, against 33 us in the segment form.
+  if (!topk_uses_workspace(rows, p.ld) && (RS.total > kSmemLimit || rows * 2 <= sms)) {
+    if (rows * 4 <= sms) return launch_c<4>(p, rows, stream, pdl);
+    if (rows * 2 <= sms) return launch_c<2>(p, rows, stream, pdl);
+    return launch_c<1>(p, rows, stream, pdl);
+  }
+  cudaError_t e;
+  if (!topk_uses_workspace(rows, p.ld)) topk_set_workspace(p, nullptr);
+  if (p.ghist != nullptr) {
+    // segments: 16K positions, fewer when that leaves most SMs idle
+    const int sms = num_sms() > 0 ? num_sms() : 148;
+    p.seg_quads = 4096;
+    while (p.seg_quads > 1024 &&
+           static_cast<long long>(rows) * ((p.ld + 4LL * p.seg_quads - 1) / (4LL * p.seg_quads)) <
+               2LL * sms)
+      p.seg_quads /= 2;
+    const dim3 grid(static_cast<unsigned>((p.ld + 4LL * p.seg_quads - 1) / (4LL * p.seg_quads)),
+                    static_cast<unsigned>(rows));
+    e = launch_ex(topk_hist_kernel, grid, dim3(kSThreads), 0, stream, pdl, p);
+    if (e != cudaSuccess) return e;
+    e = launch_ex(topk_mark_kernel, grid, dim3(kSThreads), 0, stream, true, p);
+    if (e != cudaSuccess) return e;
+    pdl = true;
+  }
+  e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RS.total);
+  if (e != cudaSuccess) return e;
+  return launch_ex(topk_rows_kernel, dim3(rows), dim3(kRThreads), RS.total, stream, pdl, p, RS);
 }
 
 }  // namespace dsa

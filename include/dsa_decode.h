@@ -68,7 +68,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 1
+#define DSA_ABI_VERSION 2
 
 /* fixed geometry */
 #define DSA_INDEX_HEADS 64   /* indexer heads per query row */
@@ -193,6 +193,12 @@ int dsa_indexer_scores(const uint16_t* q_idx, const float* w_idx,
                        int64_t ld_scores, int32_t* d_err, void* stream);
 
 /*
+ * Workspace bytes dsa_topk uses for its segment-parallel form on num_rows
+ * score rows of stride ld_scores (0 for num_rows <= 0 or a bad stride).
+ */
+size_t dsa_topk_workspace_size(int32_t num_rows, int64_t ld_scores);
+
+/*
  * dsa_topk -- exact top-k of every score row (DCP page, Motivation: the top
  * 2048 tokens of the whole sequence).
  *
@@ -207,14 +213,24 @@ int dsa_indexer_scores(const uint16_t* q_idx, const float* w_idx,
  *   out_score: device fp32 [num_rows][k] or NULL: the selected scores, same
  *              order (entries past the count are -inf)
  *   out_count: device int32 [num_rows]: min(k, valid_len[r])
- * -0.0 and +0.0 are equal scores.  A NaN score sets DSA_DEVERR_NAN.
+ *   workspace: device, >= dsa_topk_workspace_size(num_rows, ld_scores)
+ *              bytes, 16-byte aligned, or NULL.  With it the passes over the
+ *              scores are split into segments spread over every SM (three
+ *              launches; the call first clears the workspace's histograms
+ *              on `stream`); without it one CTA per row does every pass
+ *              (one launch, slower when rows are few or long).  The result
+ *              is the same.  DSA_ERR_WORKSPACE_TOO_SMALL when workspace_bytes
+ *              is below the size.
+ * -0.0 and +0.0 are equal scores (a selected -0.0 is listed in out_score as
+ * +0.0).  A NaN score sets DSA_DEVERR_NAN.
  * index_stride/index_offset turn shard-local positions into global ones
  * (stride = W, offset = shard); pass 1 and 0 otherwise.
  */
 int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* valid_len,
              int32_t num_rows, int32_t k, int32_t index_stride,
              int32_t index_offset, int32_t* out_idx, float* out_score,
-             int32_t* out_count, int32_t* d_err, void* stream);
+             int32_t* out_count, void* workspace, size_t workspace_bytes,
+             int32_t* d_err, void* stream);
 
 /*
  * dsa_shard_topk_merge -- exact global top-k from per-shard local top-k
@@ -440,6 +456,7 @@ typedef struct {
   int64_t ld_scores;
   int64_t cand_idx, cand_score, cand_count;
   int64_t topk_idx, topk_count;
+  int64_t topk_ws;  /* the top-k's own workspace (histograms, candidates, bitmaps) */
   int64_t owned_local, owned_count;
   int64_t part_out, part_lse;
   int32_t num_splits;

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.dsa_abi_version() == 1
+    assert lib.dsa_abi_version() == 2
     for s in range(7):
         assert lib.dsa_status_string(s).startswith(b"DSA_")
     assert lib.dsa_status_string(99) == b"unknown dsa status"
@@ -49,11 +49,20 @@ def test_host_validation_rejects_bad_arguments(lib):
     err = ctypes.c_void_p(16)  # never dereferenced: validation fails first
     # k out of range
     assert lib.dsa_topk(ctypes.c_void_p(16), 10, ctypes.c_void_p(16), 1, 0, 1, 0,
-                        ctypes.c_void_p(16), None, ctypes.c_void_p(16), err, None) == C.DSA_ERR_INVALID_ARG
+                        ctypes.c_void_p(16), None, ctypes.c_void_p(16), None, 0, err,
+                        None) == C.DSA_ERR_INVALID_ARG
     assert lib.dsa_topk(ctypes.c_void_p(16), 10, ctypes.c_void_p(16), 1, 5000, 1, 0,
-                        ctypes.c_void_p(16), None, ctypes.c_void_p(16), err, None) == C.DSA_ERR_INVALID_ARG
+                        ctypes.c_void_p(16), None, ctypes.c_void_p(16), None, 0, err,
+                        None) == C.DSA_ERR_INVALID_ARG
+    # a workspace below the size
+    need = lib.dsa_topk_workspace_size(3, 5000)
+    assert need > 0
+    assert lib.dsa_topk(ctypes.c_void_p(16), 5000, ctypes.c_void_p(16), 3, 64, 1, 0,
+                        ctypes.c_void_p(16), None, ctypes.c_void_p(16), ctypes.c_void_p(256),
+                        need - 1, err, None) == C.DSA_ERR_WORKSPACE_TOO_SMALL
     # zero rows: nothing to do, no CUDA call
-    assert lib.dsa_topk(None, 10, None, 0, 64, 1, 0, None, None, None, err, None) == C.DSA_OK
+    assert lib.dsa_topk(None, 10, None, 0, 64, 1, 0, None, None, None, None, 0, err,
+                        None) == C.DSA_OK
     # unsupported head count
     cache = C.DsaPagedCache(data=16, scale=None, block_table=None, dtype=0, row_elems=576,
                             page_size=64, num_pages=4, max_blocks=4)

@@ -58,24 +58,43 @@ def test_indexer_single_shard_call():
 
 
 def _topk_case(s: np.ndarray, valid: np.ndarray, k: int, stride=1, offset=0):
+    """Both forms of dsa_topk (with a workspace: segments over every SM; without:
+    one CTA per row) against the oracle's selection; returns the OR of the
+    two calls' device error words."""
     R = s.shape[0]
     st = torch.from_numpy(s.astype(np.float32)).to(DEV)
     vt = torch.from_numpy(valid.astype(np.int32)).to(DEV)
-    oi = torch.full((R, k), -5, dtype=torch.int32, device=DEV)
-    os_ = torch.zeros((R, k), dtype=torch.float32, device=DEV)
-    oc = torch.zeros(R, dtype=torch.int32, device=DEV)
-    err = _err()
-    api.dsa_topk(st, vt, k, oi, oc, err, out_score=os_, index_stride=stride, index_offset=offset)
-    e = api.dsa_read_error(err)
-    oi, os_, oc = oi.cpu().numpy(), os_.cpu().numpy(), oc.cpu().numpy()
-    for r in range(R):
-        n = int(valid[r])
-        want = orc.topk_select(s[r, :n].astype(np.float32).astype(np.float64), k)
-        assert oc[r] == len(want)
-        assert np.array_equal(oi[r, : oc[r]], want * stride + offset), r
-        assert np.all(oi[r, oc[r]:] == -1)
-        assert np.array_equal(os_[r, : oc[r]], s[r, want].astype(np.float32))
+    want = [orc.topk_select(s[r, : int(valid[r])].astype(np.float32).astype(np.float64), k)
+            for r in range(R)]
+    e = 0
+    for with_ws in (True, False):
+        oi = torch.full((R, k), -5, dtype=torch.int32, device=DEV)
+        os_ = torch.zeros((R, k), dtype=torch.float32, device=DEV)
+        oc = torch.zeros(R, dtype=torch.int32, device=DEV)
+        err = _err()
+        ws = None
+        if with_ws:
+            # stale contents: the call must clear what has to start at zero
+            ws = torch.full((api.dsa_topk_workspace_size(R, s.shape[1]),), 0x5A,
+                            dtype=torch.uint8, device=DEV)
+        api.dsa_topk(st, vt, k, oi, oc, err, out_score=os_, index_stride=stride,
+                     index_offset=offset, workspace=ws)
+        e |= api.dsa_read_error(err)
+        oi_h, os_h, oc_h = oi.cpu().numpy(), os_.cpu().numpy(), oc.cpu().numpy()
+        for r in range(R):
+            assert oc_h[r] == len(want[r]), (with_ws, r)
+            assert np.array_equal(oi_h[r, : oc_h[r]], want[r] * stride + offset), (with_ws, r)
+            assert np.all(oi_h[r, oc_h[r]:] == -1), (with_ws, r)
+            assert np.array_equal(os_h[r, : oc_h[r]], s[r, want[r]].astype(np.float32)), (with_ws, r)
     return e
+
+
+def _topk_both_forms(s: np.ndarray, valid: np.ndarray, k: int, stride=1, offset=0):
+    """The rows as given (few rows: the cluster form), then repeated to 80 or
+    more rows (the segment form and its one-CTA-per-row variant)."""
+    e = _topk_case(s, valid, k, stride, offset)
+    rep = -(-80 // s.shape[0])
+    return e | _topk_case(np.tile(s, (rep, 1)), np.tile(valid, rep), k, stride, offset)
 
 
 def test_topk_random_rows():
@@ -83,7 +102,7 @@ def test_topk_random_rows():
     R, L = 6, 70000
     s = rng.standard_normal((R, L)).astype(np.float32) * 3
     valid = np.array([L, 1, 2047, 2048, 2049, 50000])
-    assert _topk_case(s, valid, 2048) == 0
+    assert _topk_both_forms(s, valid, 2048) == 0
 
 
 def test_topk_wide_and_narrow_key_ranges():
@@ -100,18 +119,33 @@ def test_topk_wide_and_narrow_key_ranges():
     s[3] = -np.exp(rng.normal(0.0, 3.0, L))
     s[4] = rng.standard_normal(L)
     valid = np.array([L, 55296, 55297, 40000, 2049])
-    assert _topk_case(s, valid, 2048) == 0
-    assert _topk_case(s, valid, 37) == 0
+    assert _topk_both_forms(s, valid, 2048) == 0
+    assert _topk_both_forms(s, valid, 37) == 0
 
 
-@pytest.mark.parametrize("R", [50, 100])
-def test_topk_cluster_widths(R):
-    """Enough rows that a row gets two CTAs (50 rows) or one (100 rows)."""
+@pytest.mark.parametrize("R", [50, 100, 400])
+def test_topk_many_rows(R):
+    """Many rows of mixed lengths: several rows share an SM, and the launch
+    runs more rows than the GPU holds at once (400)."""
     rng = np.random.default_rng(3)
     L = 40000
     s = (rng.standard_normal((R, L)) * 2 + 10).astype(np.float32)
     valid = rng.integers(1, L + 1, R)
     valid[:4] = [L, 2048, 2049, 1]
+    assert _topk_case(s, valid, 2048) == 0
+
+
+@pytest.mark.parametrize("R", [2, 45, 80])
+def test_topk_rows_too_long_for_the_bitmaps(R):
+    """Score rows of 800000 positions: the position bitmaps of one row do not
+    fit in shared memory, so a cluster of 4 (2 rows), 2 (45 rows) or 1 CTA
+    (80 rows) selects each row."""
+    rng = np.random.default_rng(5)
+    L = 800_000
+    s = (rng.standard_normal((R, L)) * 2 + 10).astype(np.float32)
+    valid = rng.integers(1, 60_000, R)
+    valid[0] = L
+    valid[1] = 2049
     assert _topk_case(s, valid, 2048) == 0
 
 
@@ -123,8 +157,8 @@ def test_topk_crowded_threshold_bin():
     s = rng.integers(0, 3, (R, L)).astype(np.float32)
     s[2] = np.where(rng.random(L) < 0.5, 7.0, 7.000001)
     valid = np.array([L, L, L])
-    assert _topk_case(s, valid, 2048) == 0
-    assert _topk_case(s, valid, 4096) == 0
+    assert _topk_both_forms(s, valid, 2048) == 0
+    assert _topk_both_forms(s, valid, 4096) == 0
 
 
 def test_topk_ties_and_signed_zero():
@@ -137,8 +171,8 @@ def test_topk_ties_and_signed_zero():
     s[3, ::7] = 2.0                             # 1286 twos, ties at the k-th place
     s[4] = np.round(rng.standard_normal(L), 1)
     valid = np.full(R, L)
-    assert _topk_case(s, valid, 2048) == 0
-    assert _topk_case(s, valid, 100, stride=4, offset=3) == 0
+    assert _topk_both_forms(s, valid, 2048) == 0
+    assert _topk_both_forms(s, valid, 100, stride=4, offset=3) == 0
 
 
 def test_topk_nan_flag():
