@@ -36,15 +36,15 @@
 namespace dsa {
 namespace {
 
-constexpr int kTileT = 128;
+constexpr int kBlockT = 128;  // tokens of one M-block (the M of one tcgen05 MMA)
 // 4 warps (producer, issuer, Q staging) + 4 epilogue warps per epilogue set
 __host__ __device__ constexpr int threads_of(int sets) { return 128 + 128 * sets; }
-constexpr int kOpBytes = kTileT * kIdxDim * 2;     // 32 KB bf16 key tile
-constexpr int kRawFp8Bytes = kTileT * kIdxDim;     // 16 KB e4m3 key tile
-// an fp8 stage: the e4m3 tile, then the (page, slot) of its two 64-token
-// chunks for the epilogue's scale loads, padded to the 1024-byte alignment
-// of the 128B-swizzled operand
-constexpr int kFp8StageBytes = kRawFp8Bytes + 1024;
+constexpr int kOpBytes = kBlockT * kIdxDim * 2;     // 32 KB bf16 key tile
+constexpr int kRawFp8Block = kBlockT * kIdxDim;     // 16 KB e4m3 keys of one M-block
+// an fp8 stage: the e4m3 tile (one or two M-blocks), then the (page, slot)
+// of its 64-token boxes for the epilogue's scale loads, padded to the
+// 1024-byte alignment of the 128B-swizzled operand
+__host__ __device__ constexpr int fp8_stage_bytes(int blocks) { return blocks * kRawFp8Block + 1024; }
 constexpr int kHalfBf16Box = 64 * 64 * 2;          // one TMA box: 64 tokens x 64 dims
 constexpr int kSmemLimit = 227 * 1024;
 
@@ -62,6 +62,7 @@ struct Layout {
   int off_ring, off_q, off_meta, off_rows, off_bar, total;
   int rows_smem;   // row_start and row_pos copied to shared memory (they fit)
   int slot_cols, tmem_cols, rows_per_chunk;
+  int blocks;      // M-blocks of 128 tokens per tile (2: one-row fp8 requests)
 };
 
 __host__ __device__ inline int rows_per_chunk_of(int nr) {
@@ -73,14 +74,15 @@ __host__ __device__ inline int rows_per_chunk_of(int nr) {
 // shared memory for its schedule when it fits in kRowsSmemCap bytes.
 constexpr int kRowsSmemCap = 8192;
 
-__host__ inline Layout make_layout(int fp8, int max_rows, int row_ints) {
+__host__ inline Layout make_layout(int fp8, int max_rows, int row_ints, int blocks) {
   Layout L{};
+  L.blocks = blocks;
   L.rows_smem = row_ints * 4 <= kRowsSmemCap;
   const int rows_bytes = L.rows_smem ? (row_ints * 4 + 15) / 16 * 16 : 0;
   L.q_rows = max_rows * kIdxHeads;
   L.q_kb_stride = L.q_rows * 128;
   L.rows_per_chunk = rows_per_chunk_of(max_rows);
-  L.slot_cols = L.rows_per_chunk * kIdxHeads;
+  L.slot_cols = blocks * L.rows_per_chunk * kIdxHeads;
   int cols = 32;
   while (cols < 2 * L.slot_cols) cols *= 2;
   L.tmem_cols = cols;
@@ -88,7 +90,7 @@ __host__ inline Layout make_layout(int fp8, int max_rows, int row_ints) {
   const int meta_bytes = 2 * static_cast<int>(sizeof(PairMeta));
   const int bar_bytes = 512;
   const int fixed = 1024 /*align*/ + q_bytes + meta_bytes + rows_bytes + bar_bytes;
-  L.stage_bytes = fp8 ? kFp8StageBytes : kOpBytes;
+  L.stage_bytes = fp8 ? fp8_stage_bytes(blocks) : kOpBytes;
   L.stages = (kSmemLimit - fixed) / L.stage_bytes;
   if (L.stages > 8) L.stages = 8;
   int off = 0;
@@ -133,7 +135,8 @@ struct RowMeta {
   }
 };
 
-__device__ PairInfo pair_info(const IndexerLaunch& P, const RowMeta& M, int pair, bool report) {
+__device__ PairInfo pair_info(const IndexerLaunch& P, const RowMeta& M, int pair, bool report,
+                              int tile_t) {
   const int sl = pair_shard(P, pair);
   const int b = pair_req(P, pair);
   const int g = pair % P.groups;
@@ -170,28 +173,35 @@ __device__ PairInfo pair_info(const IndexerLaunch& P, const RowMeta& M, int pair
   pi.row0 = r0;
   pi.nr = r1 - r0;
   pi.len = len;
-  pi.ntiles = (len + kTileT - 1) / kTileT;
+  pi.ntiles = (len + tile_t - 1) / tile_t;
   return pi;
 }
 
-// Walks this CTA's units in order: (pair, tile).
+// Walks this CTA's units in order: (pair, tile).  The pair's shard and
+// request are kept, so that a tile needs no division.
 struct Walker {
-  int pair, tile, npairs;
+  int pair, tile, npairs, tile_t, sl, b;
   PairInfo pi;
   RowMeta M;
-  __device__ void start(const IndexerLaunch& P, const RowMeta& m, int p, int t) {
+  __device__ void start(const IndexerLaunch& P, const RowMeta& m, int p, int t, int tt) {
     M = m;
     pair = p;
     tile = t;
+    tile_t = tt;
     npairs = P.nshards * P.num_reqs * P.groups;
-    pi = pair_info(P, M, pair, false);
+    set_pair(P);
     skip(P);
+  }
+  __device__ void set_pair(const IndexerLaunch& P) {
+    pi = pair_info(P, M, pair, false, tile_t);
+    sl = pair_shard(P, pair);
+    b = pair_req(P, pair);
   }
   __device__ void skip(const IndexerLaunch& P) {
     while (tile >= pi.ntiles && pair + 1 < npairs) {
       ++pair;
       tile = 0;
-      pi = pair_info(P, M, pair, false);
+      set_pair(P);
     }
   }
   __device__ void next(const IndexerLaunch& P) {
@@ -204,6 +214,11 @@ __device__ __forceinline__ int page_of(const IndexerLaunch& P, int sl, int b, in
   const int32_t* bt = P.block_table[sl];
   return bt ? __ldg(bt + static_cast<long long>(b) * P.max_blocks[sl] + lp)
             : b * P.max_blocks[sl] + lp;
+}
+
+// logical page of token t (a shift when the page size is a power of two)
+__device__ __forceinline__ int page_of_token(const IndexerLaunch& P, int t) {
+  return P.page_shift >= 0 ? (t >> P.page_shift) : t / P.page_size;
 }
 
 // Two e4m3 terms of a float pair (a, b): hi = e4m3(x), lo = e4m3(x - hi),
@@ -219,10 +234,15 @@ __device__ __forceinline__ void split_e4m3x2(float a, float b, uint32_t& hi, uin
   lo = static_cast<uint32_t>(l);
 }
 
-template <bool kFp8, int kSets>
+template <bool kFp8, int kSets, int kBlocks>
 __global__ void __launch_bounds__(threads_of(kSets), 1)
     indexer_kernel(const __grid_constant__ IndexerLaunch P, const Layout L) {
   constexpr int kThreads = threads_of(kSets);
+  constexpr int kTileT = kBlockT * kBlocks;  // tokens per tile
+  constexpr int kBoxes = kTileT / 64;        // 64-token TMA boxes per tile
+  static_assert(kBlocks == 1 || (kFp8 && kSets == 2), "two-block tiles: fp8 keys, two sets");
+  // with two-block tiles each epilogue set takes one block of every chunk
+  constexpr bool kSetPerBlock = kBlocks == 2;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -254,7 +274,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
     }
     for (int o = 0; o < 2; ++o) {
       mbar_init(bar(B_ACCFULL + o), 1);
-      mbar_init(bar(B_ACCEMPTY + o), 128);
+      mbar_init(bar(B_ACCEMPTY + o), kSetPerBlock ? 128 * kSets : 128);
       mbar_init(bar(B_PFULL + o), 1);
       mbar_init(bar(B_PEMPTY + o), 128 * kSets);
     }
@@ -309,7 +329,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
     const int p0 = min(npairs, tid * chunk);
     const int p1 = min(npairs, p0 + chunk);
     int mine = 0;
-    for (int p = p0; p < p1; ++p) mine += pair_info(P, rm, p, blockIdx.x == 0).ntiles;
+    for (int p = p0; p < p1; ++p) mine += pair_info(P, rm, p, blockIdx.x == 0, kTileT).ntiles;
     int incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -330,7 +350,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
     if (u0 < u1 && excl <= u0 && u0 < excl + mine) {
       int acc = excl;
       for (int p = p0; p < p1; ++p) {
-        const int n = pair_info(P, rm, p, false).ntiles;
+        const int n = pair_info(P, rm, p, false, kTileT).ntiles;
         if (u0 < acc + n) {
           s_start[0] = p;
           s_start[1] = static_cast<int>(u0 - acc);
@@ -359,7 +379,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
       // the pages of 16 tiles) and handed to lane 0 by a shuffle, so that a
       // tile waits for no global load of its own.
       Walker wk;
-      wk.start(P, rm, start_pair, start_tile);
+      wk.start(P, rm, start_pair, start_tile, kTileT);
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -370,12 +390,13 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
             lane == 0 ? mbar_wait(bar(B_KEMPTY + stage), phase ^ 1u, abort_flag) : true, 0);
         if (!got) break;
         ++issued;
-        const int sl = pair_shard(P, wk.pair);
-        const int b = pair_req(P, wk.pair);
+        const int sl = wk.sl;
+        const int b = wk.b;
         const int32_t* bt = P.block_table[sl];
         const int t0 = wk.tile * kTileT;
-        const int lpa = t0 / P.page_size;  // the tile's first page
-        if (bt != nullptr && (wk.pair != pc_pair || lpa < pc_base || lpa + 1 >= pc_base + 32)) {
+        const int lpa = page_of_token(P, t0);                // the tile's first page
+        const int lpz = page_of_token(P, t0 + kTileT - 1);   // and its last
+        if (bt != nullptr && (wk.pair != pc_pair || lpa < pc_base || lpz >= pc_base + 32)) {
           pc_pair = wk.pair;
           pc_base = lpa;
           const int e = pc_base + lane;
@@ -383,11 +404,14 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
                        ? __ldg(bt + static_cast<long long>(b) * P.max_blocks[sl] + e)
                        : -1;
         }
-        int pages[2] = {-1, -1}, slots[2] = {0, 0};
+        int pages[kBoxes], slots[kBoxes];
         uint32_t bytes = 0;
-        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int h = 0; h < kBoxes; ++h) {
+          pages[h] = -1;
+          slots[h] = 0;
           const int th = t0 + h * 64;
-          const int lp = th / P.page_size;
+          const int lp = page_of_token(P, th);
           const int cached = __shfl_sync(0xffffffffu, pc_val, (lp - pc_base) & 31);
           if (th >= wk.pi.len) continue;
           const int pg = bt != nullptr ? cached : b * P.max_blocks[sl] + lp;
@@ -396,7 +420,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
             continue;
           }
           pages[h] = pg;
-          slots[h] = th % P.page_size;
+          slots[h] = th - lp * P.page_size;
           bytes += kFp8 ? 64u * 128u : 2u * kHalfBf16Box;
         }
         if (lane == 0) {
@@ -404,16 +428,19 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
           const uint32_t dst = ring + stage * L.stage_bytes;
           if (kFp8) {
             // where the epilogue finds the tile's token scales (it loads its
-            // token's scale itself); released to it by the arrival below
+            // token's scale itself): the boxes' pages, then their first
+            // slots; released to it by the arrival below
             int* where = reinterpret_cast<int*>(sbase + L.off_ring + stage * L.stage_bytes +
-                                                kRawFp8Bytes);
-            where[0] = pages[0];
-            where[1] = pages[1];
-            where[2] = slots[0];
-            where[3] = slots[1];
+                                                kBlocks * kRawFp8Block);
+#pragma unroll
+            for (int h = 0; h < kBoxes; ++h) {
+              where[h] = pages[h];
+              where[kBoxes + h] = slots[h];
+            }
           }
           mbar_arrive_expect_tx(fb, bytes);
-          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int h = 0; h < kBoxes; ++h) {
             if (pages[h] < 0) continue;
             if (kFp8) {
               tma_load_3d(dst + h * 8192, &P.kmap[sl], fb, 0, slots[h], pages[h]);
@@ -453,7 +480,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
       // ------------------------------------------------ MMA issuer
       if (lane == 0) {
         Walker wk;
-        wk.start(P, rm, start_pair, start_tile);
+        wk.start(P, rm, start_pair, start_tile, kTileT);
         int stage = 0;
         uint32_t phase = 0;
         uint32_t acc_iter = 0;
@@ -481,24 +508,34 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
               break;
             }
             tc_fence_after();
-            const uint32_t d = tmem_base + static_cast<uint32_t>(slot * L.slot_cols);
             const uint32_t idesc = kFp8 ? idesc_e4m3(128, rows_c * kIdxHeads)
                                         : idesc_f16(128, rows_c * kIdxHeads, 1, 1);
-            const uint32_t b_base = qbase + static_cast<uint32_t>(c0 * kIdxHeads * 128);
-            // bf16: kb walks the two 64-dim halves of keys and query.
-            // fp8: the 128-dim e4m3 tile is one 128-byte row per token, met
-            // once by the hi terms of the query (kb 0) and once by the lo
-            // terms (kb 1), both into the same accumulator.
+            // descriptors: the start address field (bits 0..13, in 16-byte
+            // units) of the block's first K-step, stepped by adding offsets
+            const uint64_t bd0 =
+                smem_desc_sw128(qbase + static_cast<uint32_t>(c0 * kIdxHeads * 128));
 #pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
+            for (int blk = 0; blk < kBlocks; ++blk) {
+              // block blk: tokens blk * 128 .. + 127 of the tile, its own
+              // accumulator columns in the slot
+              const uint32_t d = tmem_base + static_cast<uint32_t>(
+                                                 slot * L.slot_cols + blk * rpc * kIdxHeads);
+              const uint64_t ad0 = smem_desc_sw128(a_base + blk * kRawFp8Block);
+              // bf16: kb walks the two 64-dim halves of keys and query.
+              // fp8: the 128-dim e4m3 block is one 128-byte row per token, met
+              // once by the hi terms of the query (kb 0) and once by the lo
+              // terms (kb 1), both into the same accumulator.
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t ad = smem_desc_sw128(a_base + (kFp8 ? 0 : kb * 16384) + k * 32);
-                const uint64_t bd = smem_desc_sw128(b_base + kb * L.q_kb_stride + k * 32);
-                if (kFp8)
-                  tc_mma_f8(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-                else
-                  tc_mma_f16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t ad = ad0 + static_cast<uint64_t>(((kFp8 ? 0 : kb * 16384) + k * 32) >> 4);
+                  const uint64_t bd = bd0 + static_cast<uint64_t>((kb * L.q_kb_stride + k * 32) >> 4);
+                  if (kFp8)
+                    tc_mma_f8(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                  else
+                    tc_mma_f16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                }
               }
             }
             tc_commit(bar(B_ACCFULL + slot));
@@ -520,7 +557,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
       // ------------------------------------------------ Q staging
       const int at = tid - 64;  // 0..63
       Walker wk;
-      wk.start(P, rm, start_pair, start_tile);
+      wk.start(P, rm, start_pair, start_tile, kTileT);
       int pair_j = -1, last_pair = -1;
       // A failed (timed-out) wait stops the work of this thread but it keeps
       // passing the same named barriers as its partner warp.
@@ -622,14 +659,16 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
       }
     } else {
       // ------------------------------------------------ epilogue (warps 4..)
-      // With two sets of four warps each takes one accumulator slot: set 0
-      // (warps 4..7) the chunks that land in slot 0, set 1 (warps 8..11)
-      // those in slot 1, so two chunks are summed at once.
-      const int et = (tid - 128) & 127;    // token row of the tile / TMEM lane
+      // With two sets of four warps and one-block tiles each set takes one
+      // accumulator slot: set 0 (warps 4..7) the chunks that land in slot 0,
+      // set 1 (warps 8..11) those in slot 1, so two chunks are summed at
+      // once.  With two-block tiles set e takes block e of every chunk.
+      const int eset = (warp - 4) >> 2;    // this warp's set
+      const int eblk = kSetPerBlock ? eset : 0;  // the block of the tile it reads
+      const int et = (tid - 128) & 127;    // token row of the block / TMEM lane
       const int q4 = warp & 3;             // TMEM lane quarter of this warp
-      const int eset = (warp - 4) >> 2;    // the accumulator slot this set reads
       Walker wk;
-      wk.start(P, rm, start_pair, start_tile);
+      wk.start(P, rm, start_pair, start_tile, kTileT);
       uint32_t acc_iter = 0;
       int stage = 0;
       uint32_t phase = 0;
@@ -644,8 +683,9 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
           if (!__all_sync(0xffffffffu, got)) break;
         }
         const PairMeta& m = meta[pair_j & 1];
-        const int sl = pair_shard(P, wk.pair);
-        const int t = wk.tile * kTileT + et;
+        const int sl = wk.sl;
+        const int tt = eblk * kBlockT + et;  // token of the tile
+        const int t = wk.tile * kTileT + tt;
         // With two sets both wait for the tile's keys, also the set without
         // a chunk in it: its release of the stage must not run ahead of the
         // fill (it would count towards the stage's previous use).
@@ -657,12 +697,12 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
         if (kFp8) {
           // the token's scale, from the (page, slot) the producer left behind
           // the keys; loaded now, used after the accumulator wait
-          const int* where = reinterpret_cast<const int*>(sbase + L.off_ring +
-                                                          stage * L.stage_bytes + kRawFp8Bytes);
-          const int h = et >> 6;
+          const int* where = reinterpret_cast<const int*>(
+              sbase + L.off_ring + stage * L.stage_bytes + kBlocks * kRawFp8Block);
+          const int h = tt >> 6;
           const int pg = where[h];
           kscale = pg >= 0 ? __ldg(P.kscale[sl] + static_cast<long long>(pg) * P.page_size +
-                                   where[2 + h] + (et & 63))
+                                   where[kBoxes + h] + (tt & 63))
                            : 0.0f;
         }
         float* out_base = P.scores + static_cast<long long>(sl) * P.shard_stride;
@@ -673,7 +713,7 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
           const int rows_c = min(rpc, nr - c0);
           const int slot = static_cast<int>(acc_iter & 1u);
           const uint32_t aph = (acc_iter >> 1) & 1u;
-          if (kSets == 2 && slot != eset) {  // the other set's chunk
+          if (kSets == 2 && !kSetPerBlock && slot != eset) {  // the other set's chunk
             ++acc_iter;
             continue;
           }
@@ -684,8 +724,9 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
           tc_fence_after();
           for (int gi = 0; gi < rows_c; ++gi) {
             const int g = c0 + gi;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) +
-                                   static_cast<uint32_t>(slot * L.slot_cols + gi * kIdxHeads);
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(q4 * 32) << 16) +
+                static_cast<uint32_t>(slot * L.slot_cols + (eblk * rpc + gi) * kIdxHeads);
             uint32_t v0[32], v1[32];
             tmem_ld_32x32b_x32(taddr, v0);
             tmem_ld_32x32b_x32(taddr + 32, v1);
@@ -733,19 +774,27 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
 }
 
 
-template <bool kFp8, int kSets>
+template <bool kFp8, int kSets, int kBlocks>
 cudaError_t launch_one(const IndexerLaunch& p, const Layout& L, int grid, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(indexer_kernel<kFp8, kSets>,
+  cudaError_t e = cudaFuncSetAttribute(indexer_kernel<kFp8, kSets, kBlocks>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return e;
-  indexer_kernel<kFp8, kSets><<<grid, threads_of(kSets), L.total, stream>>>(p, L);
+  indexer_kernel<kFp8, kSets, kBlocks><<<grid, threads_of(kSets), L.total, stream>>>(p, L);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_indexer(const IndexerLaunch& p, cudaStream_t stream) {
-  const Layout L = make_layout(p.fp8, p.max_rows, p.num_reqs + 1 + p.num_rows);
+cudaError_t launch_indexer(const IndexerLaunch& p0, cudaStream_t stream) {
+  IndexerLaunch p = p0;
+  p.page_shift = -1;
+  for (int s = 6; s < 31; ++s)
+    if (p.page_size == (1 << s)) p.page_shift = s;
+  // one-row fp8 requests: 256-token tiles (two M-blocks), so that a tile
+  // carries as many key bytes as a bf16 tile and the per-tile work of every
+  // role is paid per 32 KB
+  const int blocks = (p.fp8 && p.max_rows == 1) ? 2 : 1;
+  const Layout L = make_layout(p.fp8, p.max_rows, p.num_reqs + 1 + p.num_rows, blocks);
   if (L.stages < 2) return cudaErrorInvalidValue;
   int grid = num_sms();
   if (grid <= 0) return cudaErrorInvalidDevice;
@@ -753,9 +802,11 @@ cudaError_t launch_indexer(const IndexerLaunch& p, cudaStream_t stream) {
   // keys (a scale load per token, half the key bytes per tile) or several
   // rows per request; for one bf16 row the MMA issue is the bound and the
   // extra warps only crowd the issuing thread's sub-partition.
-  if (p.fp8) return launch_one<true, 2>(p, L, grid, stream);
-  if (p.max_rows > 1) return launch_one<false, 2>(p, L, grid, stream);
-  return launch_one<false, 1>(p, L, grid, stream);
+  if (p.fp8)
+    return blocks == 2 ? launch_one<true, 2, 2>(p, L, grid, stream)
+                       : launch_one<true, 2, 1>(p, L, grid, stream);
+  if (p.max_rows > 1) return launch_one<false, 2, 1>(p, L, grid, stream);
+  return launch_one<false, 1, 1>(p, L, grid, stream);
 }
 
 }  // namespace dsa

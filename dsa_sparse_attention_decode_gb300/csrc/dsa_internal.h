@@ -21,6 +21,7 @@ struct IndexerLaunch {
   int32_t num_pages[DSA_MAX_SHARDS];
   int32_t max_blocks[DSA_MAX_SHARDS];
   int32_t page_size;
+  int32_t page_shift;   // log2(page_size) when a power of two, else -1 (set by the launcher)
   int32_t fp8;
   int32_t W;            // shards of the group
   int32_t shard_base;   // id of kmap[0]
