@@ -128,6 +128,22 @@ cudaError_t make_index_k_tmap(CUtensorMap* map, const dsa_paged_cache& c) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_kv_fp8_tmap(CUtensorMap* map, const void* data, int num_pages, int page_size) {
+  auto enc = get_encode();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  // the cache as [pages * page_size rows][576] e4m3; 128-byte column boxes of
+  // one row, gathered four rows at a time
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kKvDim),
+                        static_cast<cuuint64_t>(num_pages) * static_cast<cuuint64_t>(page_size)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kKvDim)};
+  cuuint32_t box[2] = {128u, 1u};
+  cuuint32_t estride[2] = {1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(data), gdim, gstride,
+                   box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace dsa
 
 using namespace dsa;

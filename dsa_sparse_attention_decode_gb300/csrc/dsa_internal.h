@@ -138,6 +138,13 @@ struct MlaLaunch {
 // for the previous grid, which therefore must not write them
 cudaError_t launch_sparse_mla(const MlaLaunch& p, cudaStream_t stream, bool pdl = false);
 int auto_mla_splits(int work_rows, int k, int expected_count);
+// the tensor-core form for fp8 caches with 32 heads (tiles of 128 tokens):
+// launch_sparse_mla takes it when sparse_mla_tc_supported(p)
+bool sparse_mla_tc_supported(const MlaLaunch& p);
+cudaError_t launch_sparse_mla_tc(const MlaLaunch& p, cudaStream_t stream, bool pdl);
+// Host: the TMA map of an fp8 latent cache as [num_pages * page_size][576]
+// rows with 128-byte column boxes of one row (for tile::gather4 loads)
+cudaError_t make_kv_fp8_tmap(CUtensorMap* map, const void* data, int num_pages, int page_size);
 
 // ------------------------------------------------------------- cache write
 

@@ -665,6 +665,7 @@ int auto_mla_splits(int work_rows, int k, int expected_count) {
 
 cudaError_t launch_sparse_mla(const MlaLaunch& p0, cudaStream_t stream, bool pdl) {
   if (p0.nshards * p0.rows == 0 || p0.num_splits == 0) return cudaSuccess;
+  if (sparse_mla_tc_supported(p0)) return launch_sparse_mla_tc(p0, stream, pdl);
   // keep a request's block-table row in shared memory when it is short
   // enough and fits beside the tiles
   MlaLaunch p = p0;

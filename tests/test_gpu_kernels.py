@@ -291,6 +291,46 @@ def test_sparse_mla_prefill_into(cfg):
             assert np.all(m_all[r] >= l_all[r] - np.log(cnt[r]) - 1e-5)
 
 
+def test_sparse_mla_running_max_moves_fp8():
+    """fp8 latent rows whose token scales are multiplied by 1, 10 and 30 in
+    runs of 128 selected rows (one tensor-core tile): the maximum logit of
+    every head jumps by several nats from one tile to the next, so the
+    running maxima must move and the accumulated output be rescaled."""
+    wl = make_workload(config_spec(2, B=2, L_lo=2500, L_hi=4000))
+    rng = np.random.default_rng(12)
+    k = 2048
+    idx = np.zeros((wl.R, k), np.int32)
+    cnt = np.zeros(wl.R, np.int32)
+    c = wl.kv
+    for r in range(wl.R):
+        n = min(k, int(wl.row_pos[r]) + 1)
+        idx[r, :n] = rng.choice(int(wl.row_pos[r]) + 1, n, replace=False).astype(np.int32)
+        cnt[r] = n
+    # the same token is selected by several rows of a request: scale tokens by
+    # their rank in row 0 of the request, so every row sees jumps
+    for b in range(wl.B):
+        r0 = int(wl.row_start[b])
+        for rank, t in enumerate(idx[r0, : cnt[r0]]):
+            f = (1.0, 10.0, 30.0)[(rank // 128) % 3]
+            pg, sl = c.physical_page(b, int(t) // c.page_size), int(t) % c.page_size
+            c.scale[pg, sl] *= np.float32(f)
+    dw = upload(wl, DEV)
+    t_ = lambda a: torch.from_numpy(a).to(DEV)  # noqa: E731
+    for S in (0, 1, 3):
+        out = torch.zeros((wl.R, wl.H, 512), device=DEV)
+        lse = torch.zeros((wl.R, wl.H), device=DEV)
+        ws = torch.zeros(max(api.dsa_sparse_mla_decode_workspace_size(wl.R, wl.H, k, S), 1),
+                         dtype=torch.uint8, device=DEV)
+        err = _err()
+        api.dsa_sparse_mla_decode(dw.q, wl.sm_scale, dw.kv, dw.rows, t_(idx), t_(cnt), out, lse,
+                                  err, workspace=ws, num_splits=S)
+        assert api.dsa_read_error(err) == 0
+        for r in range(wl.R):
+            O_ref, l_ref = orc.row_attention(wl, r, idx[r, : cnt[r]])
+            eo, el = attn_err(out[r].cpu().numpy(), lse[r].cpu().numpy(), O_ref, l_ref)
+            assert eo <= 5e-3 and el <= 1e-4, (S, r, eo, el)
+
+
 @pytest.mark.parametrize("cfg", [0, 1])
 def test_sparse_mla_running_max_moves(cfg):
     """Selected rows scaled by 1, 10 and 30 tile by tile (64 tokens, in list
