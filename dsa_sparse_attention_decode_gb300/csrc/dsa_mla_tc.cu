@@ -50,8 +50,9 @@ namespace {
 
 constexpr int kH = 32;                   // heads
 constexpr int kT = 128;                  // tokens per tile (the M of S^T)
-constexpr int kThreads = 416;   // warps 0-3 gather, 4-11 softmax, 12 MMA
+constexpr int kThreads = 448;   // warps 0-3 gather, 4-11 softmax, 12 MMA, 13 scales
 constexpr int kMmaWarp = 12;
+constexpr int kScaleWarp = 13;
 constexpr int kSmx = 256;       // softmax threads
 constexpr int kHH = kH / 2;     // heads of one softmax thread
 constexpr int kBoxes = 5;                // 128-byte column boxes of a latent row
@@ -68,10 +69,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kOffKV = 0;                              // 2 tiles
 constexpr int kOffQ = kOffKV + 2 * kTileBytes;         // hi, lo
 constexpr int kOffP = kOffQ + 2 * kQBytes;             // [slot][hi, lo]
-constexpr int kOffKs = kOffP + 4 * kPBytes;            // [buf][128] cache rows of the tokens
-constexpr int kOffRed = kOffKs + 2 * kT * 4;           // [4 lane quarters][32] reductions
+constexpr int kOffKs = kOffP + 4 * kPBytes;            // [buf][128] token scales (-1: no token)
+constexpr int kOffRows = kOffKs + 2 * kT * 4;          // [buf][128] cache rows (-1: no token)
+constexpr int kOffRed = kOffRows + 2 * kT * 4;         // [4 lane quarters][32] reductions
 constexpr int kOffMisc = kOffRed + 4 * kH * 4;         // [32] per-head factors, flags
-constexpr int kOffBar = kOffMisc + 3 * kH * 4 + 64;
+constexpr int kOffBar = kOffMisc + 4 * kH * 4 + 64;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;       // + alignment slack
 
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -139,6 +141,21 @@ DSA_DEV float warp_transpose_reduce16(float* v, int lane) {
   return kMax ? fmaxf(v[0], o) : v[0] + o;
 }
 
+// named barrier `id` of `n` threads that also ORs a predicate over them
+DSA_DEV bool named_bar_or(int id, int n, int pred) {
+  uint32_t r;
+  __syncwarp();  // the .aligned form needs a converged warp
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %3, 0;\n\t"
+      "bar.red.or.pred q, %1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(id), "r"(n), "r"(pred)
+      : "memory");
+  return r != 0;
+}
+
 DSA_DEV void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {
   __syncwarp();  // the .aligned form needs a converged warp
   asm volatile(
@@ -186,20 +203,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sb + kOffBar);
   // barriers: KV_FULL[2], KV_EMPTY[2], S_FULL[2], S_EMPTY[2], P_FULL[2], O_FULL
   auto bar = [&](int i) { return smem_u32(bars + i); };
-  const int B_KVF = 0, B_KVE = 2, B_SF = 4, B_SE = 6, B_PF = 8, B_OF = 10, B_DRAIN = 11;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 12);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
-  int* misc_i = reinterpret_cast<int*>(bars + 14);  // [0] request index
+  const int B_KVF = 0, B_KVE = 2, B_SF = 4, B_SE = 6, B_PF = 8, B_OF = 10, B_DRAIN = 11,
+            B_ROWS = 12;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  int* misc_i = reinterpret_cast<int*>(bars + 16);  // [0] request index
   float* qexp = reinterpret_cast<float*>(sb + kOffMisc);  // [32] logit factor per head
   float* lsum = qexp + kH;                                // [32] denominators
   float* Ms = lsum + kH;                                  // [32] running maxima of a
+  float* Mn = Ms + kH;                                    // [32] their candidates for a tile
   float* red = reinterpret_cast<float*>(sb + kOffRed);    // [4][32]
-  int* rows_s = reinterpret_cast<int*>(sb + kOffKs);     // [2][128] cache row (or -1)
+  float* ks_s = reinterpret_cast<float*>(sb + kOffKs);    // [2][128] token scales
+  int* rows_s = reinterpret_cast<int*>(sb + kOffRows);    // [2][128] cache rows
 
   pdl_trigger();
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_KVF + i), 32);   // every gather lane: its copies and scales
+      mbar_init(bar(B_KVF + i), 64);   // every gather lane (its copies), every scale lane
+      mbar_init(bar(B_ROWS + i), 32);  // every gather lane wrote its rows
       mbar_init(bar(B_KVE + i), 1);    // MMA commit after the tile's value product
       mbar_init(bar(B_SF + i), 1);     // MMA commit after S^T
       mbar_init(bar(B_SE + i), kSmx);  // softmax threads read S^T
@@ -357,10 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           const uint32_t full = bar(B_KVF + buf);
+          // the rows go to the scale warp, which loads the token scales
           *reinterpret_cast<int4*>(rows_s + buf * kT + 4 * g) =
               make_int4(rows[0] == oob ? -1 : rows[0], rows[1] == oob ? -1 : rows[1],
                         rows[2] == oob ? -1 : rows[2], rows[3] == oob ? -1 : rows[3]);
-          // the rows are released by this arrival; the copies complete on it
+          mbar_arrive(bar(B_ROWS + buf));
           mbar_arrive_expect_tx(full, kBoxes * 512u);
           const uint32_t dst = base + kOffKV + buf * kTileBytes + g * 512;
 #pragma unroll
@@ -381,6 +403,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         volatile int no_abort = 0;
         for (int tile = max(0, issued - 2); tile < issued; ++tile)
           mbar_wait(bar(B_KVF + (tile & 1)), static_cast<uint32_t>(tile >> 1) & 1u, &no_abort);
+      }
+    } else if (warp == kScaleWarp) {
+      // ================================================= token scales
+      // For every tile, once its rows are known: 4 tokens' scales per lane,
+      // released to the softmax by the arrival on the tile's full barrier.
+      for (int tile = 0; tile < ntiles; ++tile) {
+        const int buf = tile & 1;
+        if (!mbar_wait(bar(B_ROWS + buf), static_cast<uint32_t>(tile >> 1) & 1u, abort_flag)) break;
+        const int4 rw = *reinterpret_cast<const int4*>(rows_s + buf * kT + 4 * lane);
+        const int r4[4] = {rw.x, rw.y, rw.z, rw.w};
+        float ks[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ks[q] = r4[q] >= 0 ? __ldg(P.kscale[w] + r4[q]) : -1.0f;
+        *reinterpret_cast<float4*>(ks_s + buf * kT + 4 * lane) = make_float4(ks[0], ks[1], ks[2], ks[3]);
+        mbar_arrive(bar(B_KVF + buf));
       }
     } else if (warp == kMmaWarp) {
       // ================================================= MMA issuer
@@ -482,12 +519,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int i = 0; i < ntiles; ++i) {
         const int buf = i & 1;
-        ok &= mbar_wait(bar(B_KVF + buf), static_cast<uint32_t>(i >> 1) & 1u, abort_flag);
-        // the token's scale (its cache row comes with the tile)
-        const int crow = rows_s[buf * kT + st];
-        const bool valid = i * kT + st < ntok && crow >= 0;
-        const float ks = valid ? __ldg(P.kscale[w] + crow) : 0.0f;
         ok &= mbar_wait(bar(B_SF + buf), static_cast<uint32_t>(i >> 1) & 1u, abort_flag);
+        // the token's scale (the MMA issuer saw the tile land before S^T)
+        ok &= mbar_wait(bar(B_KVF + buf), static_cast<uint32_t>(i >> 1) & 1u, abort_flag);
+        const float ks = ks_s[buf * kT + st];
+        const bool valid = i * kT + st < ntok && ks >= 0.0f;
         tc_fence_after();
         // a = z + log2(scale), z = sm_scale * scale * (q . code) in base 2
         float a[kHH];
@@ -515,12 +551,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane < kHH) red[wq * kH + kHH * hh + lane] = m;
         }
         named_bar_sync(1, kSmx);
-        auto new_max = [&](int h) {
-          return fmaxf(Ms[h], fmaxf(fmaxf(red[h], red[kH + h]), fmaxf(red[2 * kH + h], red[3 * kH + h])));
-        };
-        bool raise = false;  // the same for every thread
-#pragma unroll
-        for (int h = 0; h < kH; ++h) raise |= new_max(h) > Ms[h] + kLazy;
+        // thread h < 32: head h's candidate maximum; whether any head moves
+        // past the lazy margin goes to every thread with the barrier
+        int up = 0;
+        if (sid < kH) {
+          const float nm = fmaxf(Ms[sid], fmaxf(fmaxf(red[sid], red[kH + sid]),
+                                                fmaxf(red[2 * kH + sid], red[3 * kH + sid])));
+          Mn[sid] = nm;
+          up = nm > Ms[sid] + kLazy;
+        }
+        const bool raise = named_bar_or(1, kSmx, up);
+        auto new_max = [&](int h) { return Mn[h]; };
         if (raise) {
           // rescale O^T (after the previous tile's value product) and the
           // denominators to the new maxima: this thread's lane, its 16 heads
@@ -560,16 +601,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           float t[kHH];
 #pragma unroll
-          for (int h = 0; h < kHH; ++h) {
+          for (int h = 0; h < kHH; h += 2) {
             const int hg = kHH * hh + h;
-            const float mh = Ms[hg];
-            const float p = exp2f(a[h] - mh) * kPScale;
-            t[h] = exp2f(a[h] - lks - mh);  // exp2(z - M): the denominator's term
-            const uint32_t ch = e4m3_of(p);
-            const uint32_t cl = e4m3_of(p - e4m3_val(ch));
-            const int off = ((cst ^ (hg & 7)) << 4) + bst;
-            p0[hg * 128 + off] = static_cast<uint8_t>(ch);
-            p0[(kH + hg) * 128 + off] = static_cast<uint8_t>(cl);
+            const float pa = exp2f(a[h] - Ms[hg]) * kPScale;
+            const float pb = exp2f(a[h + 1] - Ms[hg + 1]) * kPScale;
+            t[h] = exp2f(a[h] - lks - Ms[hg]);  // exp2(z - M): the denominator's term
+            t[h + 1] = exp2f(a[h + 1] - lks - Ms[hg + 1]);
+            const __nv_fp8x2_storage_t c2 =
+                __nv_cvt_float2_to_fp8x2(make_float2(pa, pb), __NV_SATFINITE, __NV_E4M3);
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(c2, __NV_E4M3);
+            const float2 back = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(
+                make_float2(pa - back.x, pb - back.y), __NV_SATFINITE, __NV_E4M3);
+            const int offa = ((cst ^ (hg & 7)) << 4) + bst;
+            const int offb = ((cst ^ ((hg + 1) & 7)) << 4) + bst;
+            p0[hg * 128 + offa] = static_cast<uint8_t>(c2 & 0xFFu);
+            p0[(hg + 1) * 128 + offb] = static_cast<uint8_t>(c2 >> 8);
+            p0[(kH + hg) * 128 + offa] = static_cast<uint8_t>(l2 & 0xFFu);
+            p0[(kH + hg + 1) * 128 + offb] = static_cast<uint8_t>(l2 >> 8);
           }
           lacc += warp_transpose_reduce16<false>(t, lane);
         }
