@@ -270,7 +270,10 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
       // released by lane 0 of each epilogue warp, once each set
       // has seen the accumulators of its chunks of the tile land (the MMAs,
       // which read the stage, are then done)
-      mbar_init(bar(B_KEMPTY + s), 4 * kSets);
+      // released when the tile's MMAs complete (a commit of the issuing
+      // thread) and, for fp8 keys, once every epilogue warp has read the
+      // tile's page and slot words from the stage
+      mbar_init(bar(B_KEMPTY + s), 1 + (kFp8 ? 4 * kSets : 0));
     }
     for (int o = 0; o < 2; ++o) {
       mbar_init(bar(B_ACCFULL + o), 1);
@@ -542,6 +545,8 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
             ++acc_iter;
           }
           if (!ok) break;
+          // the stage is free for the next fill once these MMAs are done
+          tc_commit(bar(B_KEMPTY + stage));
           if (++stage == L.stages) {
             stage = 0;
             phase ^= 1u;
@@ -686,23 +691,25 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
         const int sl = wk.sl;
         const int tt = eblk * kBlockT + et;  // token of the tile
         const int t = wk.tile * kTileT + tt;
-        // With two sets both wait for the tile's keys, also the set without
-        // a chunk in it: its release of the stage must not run ahead of the
-        // fill (it would count towards the stage's previous use).
-        if (kFp8 || kSets == 2) {
-          const bool got = mbar_wait(bar(B_KFULL + stage), phase, abort_flag);
-          if (!__all_sync(0xffffffffu, got)) break;
-        }
         float kscale = 1.0f;
         if (kFp8) {
           // the token's scale, from the (page, slot) the producer left behind
-          // the keys; loaded now, used after the accumulator wait
+          // the keys; loaded now, used after the accumulator wait.  Every set
+          // reads its words once the tile has landed (also the set without a
+          // chunk in it: its arrival must not run ahead of the fill, where it
+          // would count towards the stage's previous use) and then lets the
+          // stage go.
+          const bool got = mbar_wait(bar(B_KFULL + stage), phase, abort_flag);
+          if (!__all_sync(0xffffffffu, got)) break;
           const int* where = reinterpret_cast<const int*>(
               sbase + L.off_ring + stage * L.stage_bytes + kBlocks * kRawFp8Block);
           const int h = tt >> 6;
           const int pg = where[h];
+          const int slot0 = where[kBoxes + h];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_KEMPTY + stage));
           kscale = pg >= 0 ? __ldg(P.kscale[sl] + static_cast<long long>(pg) * P.page_size +
-                                   where[kBoxes + h] + (tt & 63))
+                                   slot0 + (tt & 63))
                            : 0.0f;
         }
         float* out_base = P.scores + static_cast<long long>(sl) * P.shard_stride;
@@ -752,8 +759,6 @@ __global__ void __launch_bounds__(threads_of(kSets), 1)
           ++acc_iter;
         }
         if (!ok) break;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_KEMPTY + stage));
         if (++stage == L.stages) {
           stage = 0;
           phase ^= 1u;

@@ -6,42 +6,35 @@
 // host framework owns every device allocation, or a latency-critical path on
 // which a synchronizing cudaMalloc / cudaFree cannot be afforded.  For them
 // dsa_sparse_mla_decode_noalloc keeps the split-K partials in one fixed
-// device array that is part of the library's device image: every GPU that
-// loads the library holds DSA_NOALLOC_SCRATCH_BYTES of it until the process
-// exits, and this file never allocates or frees anything.
+// device array that is part of the library's device image, and this file
+// never allocates or frees anything itself.  The array (DSA_NOALLOC_SCRATCH_BYTES)
+// is reserved on a device when the library's device code is loaded there:
+// with CUDA's default lazy loading that is the first call of this entry point
+// on the device, so such callers should make one call at start-up, before
+// they reserve their KV pools.  It is then held until the process exits (or
+// the context is reset).
 //
 // The array is a file-scope __device__ symbol.  On the host its name is only a
-// stand-in, not a device address, so the real address is looked up once per
-// device (with that device current) through cudaGetSymbolAddress and cached;
-// that lookup happens inside the first call made on each device.
+// stand-in, not a device address, so every call looks the real address up
+// through cudaGetSymbolAddress with the call's device current.  The lookup is
+// cheap and is not cached: after a cudaDeviceReset the module may be loaded
+// again at another address, and a remembered address would then point at
+// memory this library no longer owns.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "dsa_decode.h"
 
 namespace {
 
 constexpr size_t kScratchBytes = DSA_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_scratch on the current device (looked up on first use).
+// Device address of g_scratch on the current device.
 int scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return DSA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return DSA_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return DSA_ERR_CUDA;
+  *out = p;
   return DSA_OK;
 }
 

@@ -341,13 +341,18 @@ int dsa_sparse_mla_prefill_into(const uint16_t* q, int32_t heads, float sm_scale
  *
  * Same arguments, results and errors as dsa_sparse_mla_decode.  The split-K
  * partials go to one fixed device array of DSA_NOALLOC_SCRATCH_BYTES that the
- * library image carries: every GPU that loads the library holds it until the
- * process exits, and the call never allocates or frees device memory.
+ * library's device image carries, and the call itself never allocates or
+ * frees device memory.
+ *   - The array is reserved on a device when the library's device code loads
+ *     there; with CUDA's default lazy loading that is the first call of this
+ *     entry point on the device.  Make that first call at start-up, before
+ *     reserving the KV pools and before any stream capture.  The device then
+ *     holds the array until the process exits.
  *   - Sizes whose partials do not fit (dsa_sparse_mla_decode_workspace_size()
  *     > DSA_NOALLOC_SCRATCH_BYTES) return DSA_ERR_WORKSPACE_TOO_SMALL before
  *     any launch.
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *   - Every call looks up the array's device address with the call's device
+ *     current (after a context reset the address may change).
  *   - All calls share the one array: calls whose kernels overlap on a GPU
  *     (other streams, other threads) race on it and give wrong results; order
  *     them on one stream.  The array keeps the last call's contents; nothing in
