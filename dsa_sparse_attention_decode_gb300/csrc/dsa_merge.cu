@@ -18,8 +18,11 @@ namespace {
 // The global top-k is the top-k of the union of the shards' candidate lists
 // (every token of the global top-k is in its own shard's local top-k).  One
 // 1024-thread CTA per query row:
-//   1. the exact threshold key T over the union (histograms, as for one row),
-//      ties at T going to the lowest global positions;
+//   1. the exact threshold key T over the union: 8192-bin histogram rounds
+//      over a key range that starts as the candidates' smallest to largest
+//      key (candidates all come from the upper tail of their rows, so fixed
+//      top key bits would put them into a few bins); ties at T go to the
+//      lowest global positions;
 //   2. a candidate's rank among the ties, and later its output slot, is the
 //      number of tied (selected) candidates with a lower global position in
 //      every list: per-list prefix counts + a binary search in each list,
@@ -98,29 +101,80 @@ __global__ void __launch_bounds__(kMergeThreads, 1) shard_topk_merge_kernel(cons
     }
     cnt[tid] = c;
   }
-  for (int b = tid; b < kSelBins1; b += kMergeThreads) hist[b] = 0;
   __syncthreads();
   int total = 0;
   for (int v = 0; v < W; ++v) total += cnt[v];
   const bool all = total <= k;
-  auto valid = [&](int e) { return (e % k) < cnt[e / k]; };
-  for (int e = tid; e < N; e += kMergeThreads) {
-    const int w = e / k, i = e - w * k;
-    if (i < cnt[w]) {
-      const long long g = (static_cast<long long>(w) * R + r) * k + i;
-      const uint32_t key = score_key(__ldcg(P.cand_score + g));
-      const int p = __ldcg(P.cand_pos + g);
-      if (p < 0 || p % W != w) raise_err(P.d_err, DSA_DEVERR_INDEX);
-      keys[e] = key;
-      pos[e] = p;
-      if (!all) atomicAdd(hist + (key >> kSelShift1), 1u);
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  {
+    // the candidates, 8 loads in flight per thread
+    constexpr int kU = 8;
+    for (int e0 = 0; e0 < N; e0 += kMergeThreads * kU) {
+      uint32_t key[kU];
+      int pv[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int e = e0 + u * kMergeThreads + tid;
+        const int w = e / k, i = e - w * k;
+        pv[u] = -2;
+        if (e < N && i < cnt[w]) {
+          const long long g = (static_cast<long long>(w) * R + r) * k + i;
+          key[u] = score_key(__ldcg(P.cand_score + g));
+          pv[u] = __ldcg(P.cand_pos + g);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int e = e0 + u * kMergeThreads + tid;
+        if (pv[u] == -2) continue;
+        const int w = e / k;
+        if (pv[u] < 0 || pv[u] % W != w) raise_err(P.d_err, DSA_DEVERR_INDEX);
+        keys[e] = key[u];
+        pos[e] = pv[u];
+        kmin = min(kmin, key[u]);
+        kmax = max(kmax, key[u]);
+      }
+    }
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if ((tid & 31) == 0) {
+    scratch[warp] = kmin;
+    hist[warp] = kmax;  // the histogram is not in use yet
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t a = __reduce_min_sync(0xffffffffu, scratch[tid]);
+    const uint32_t b = __reduce_max_sync(0xffffffffu, hist[tid]);
+    if (tid == 0) {
+      sh[4] = a;
+      sh[5] = b;
     }
   }
   __syncthreads();
-  uint32_t T = 0, k_rem = 0;
-  if (!all)
-    refine_threshold([&](int e) { return keys[e]; }, valid, N, static_cast<uint32_t>(k), hist,
-                     scratch, sh, T, k_rem);
+  uint32_t T = 0, k_rem = static_cast<uint32_t>(k);
+  if (!all) {
+    // [rlo, rhi] holds T; k_rem is T's rank in it from the top
+    uint32_t rlo = sh[4], rhi = sh[5];
+    __syncthreads();  // sh is read before find_bin writes it
+    auto valid = [&](int e) { return (e % k) < cnt[e / k]; };
+    while (rlo < rhi) {
+      const int shift = range_shift(rlo, rhi, 13);
+      for (int b = tid; b < kSelBins1; b += kMergeThreads) hist[b] = 0;
+      __syncthreads();
+      for (int e = tid; e < N; e += kMergeThreads) {
+        if (!valid(e)) continue;
+        const uint32_t key = keys[e];
+        if (key >= rlo && key <= rhi) atomicAdd(hist + ((key - rlo) >> shift), 1u);
+      }
+      __syncthreads();
+      find_bin(hist, kSelBins1, k_rem, scratch, sh);  // ends with a barrier
+      bin_range(rlo, rhi, shift, sh[0], &rlo, &rhi);
+      k_rem = sh[1];
+      __syncthreads();  // sh and hist are read before the next round writes them
+    }
+    T = rlo;
+  }
 
   // ranks of the ties at T, by global position
   if (warp < W) {
@@ -193,6 +247,40 @@ __global__ void __launch_bounds__(kMergeThreads, 1) shard_topk_merge_kernel(cons
 // before any is used, so the kernel waits for one round trip to L2; an
 // empty partial (LSE -inf, output not written) is skipped by selection.
 constexpr int kFastParts = 8;
+// With more partials: every thread loads a share of the parts' LSEs, a
+// block reduction gives their maximum, the live parts (LSE finite) are
+// listed in part order by a block scan with their weights exp(lse_p - m),
+// and the value dims accumulate the live partial outputs, kMergeUnroll
+// loads in flight per thread.  The order of every sum is fixed, so the
+// result does not depend on scheduling.
+constexpr int kMaxListParts = 1024;
+constexpr int kMergeUnroll = 8;
+
+// sum (kMax: maximum) of v over the CTA; every thread gets it.  red holds 33
+// words.
+template <bool kMax>
+__device__ __forceinline__ float block_reduce(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float t = __shfl_xor_sync(0xffffffffu, v, o);
+    v = kMax ? fmaxf(v, t) : v + t;
+  }
+  __syncthreads();  // red is free
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float x = lane < nw ? red[lane] : (kMax ? -__int_as_float(0x7f800000) : 0.0f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float t = __shfl_xor_sync(0xffffffffu, x, o);
+      x = kMax ? fmaxf(x, t) : x + t;
+    }
+    if (lane == 0) red[32] = x;
+  }
+  __syncthreads();
+  return red[32];
+}
 
 __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
                                  const float* __restrict__ lse_parts, int parts, int rows,
@@ -230,6 +318,74 @@ __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
         acc.y = live ? fmaf(e, v[p].y, acc.y) : acc.y;
         acc.z = live ? fmaf(e, v[p].z, acc.z) : acc.z;
         acc.w = live ? fmaf(e, v[p].w, acc.w) : acc.w;
+      }
+    }
+  } else if (parts <= kMaxListParts) {
+    __shared__ float wgt[kMaxListParts];
+    __shared__ int live[kMaxListParts];
+    __shared__ float red[33];
+    __shared__ int nlive_s;
+    const int nt = blockDim.x;
+    float lm = kNegInf;
+    for (int p = threadIdx.x; p < parts; p += nt) {
+      const float l = __ldcg(lse_parts + p * stride_p + rh);
+      wgt[p] = l;
+      lm = fmaxf(lm, l);
+    }
+    m = block_reduce<true>(lm, red);  // its barriers publish wgt
+    if (m != kNegInf) {
+      // live parts in part order: thread t takes a contiguous run of parts
+      const int per = (parts + nt - 1) / nt;
+      const int p0 = min(parts, static_cast<int>(threadIdx.x) * per), p1 = min(parts, p0 + per);
+      int mine = 0;
+      float dsum = 0.0f;
+      for (int p = p0; p < p1; ++p) {
+        const float l = wgt[p];
+        if (l != kNegInf) {
+          ++mine;
+          dsum += expf(l - m);
+        }
+      }
+      // exclusive scan of the live counts over the threads
+      int incl = mine;
+      const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      __shared__ int wsum[32];
+      if (lane == 31) wsum[warp] = incl;
+      __syncthreads();
+      int off = incl - mine;
+      for (int w2 = 0; w2 < warp; ++w2) off += wsum[w2];
+      if (threadIdx.x == nt - 1) nlive_s = off + mine;
+      __syncthreads();  // every thread has read wsum and the raw LSEs of its run
+      for (int p = p0; p < p1; ++p) {
+        const float l = wgt[p];
+        if (l != kNegInf) live[off++] = p;
+      }
+      den = block_reduce<false>(dsum, red);  // its barriers publish live
+      const int nl = nlive_s;
+      if (has_d) {
+        for (int i0 = 0; i0 < nl; i0 += kMergeUnroll) {
+          float4 v[kMergeUnroll];
+          float e[kMergeUnroll];
+#pragma unroll
+          for (int u = 0; u < kMergeUnroll; ++u) {
+            const int p = i0 + u < nl ? live[i0 + u] : -1;
+            e[u] = p >= 0 ? expf(__ldcg(lse_parts + p * stride_p + rh) - m) : 0.0f;
+            v[u] = p >= 0 ? __ldcg(reinterpret_cast<const float4*>(O_parts + (p * stride_p + rh) * dv) + d4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < kMergeUnroll; ++u) {
+            acc.x = fmaf(e[u], v[u].x, acc.x);
+            acc.y = fmaf(e[u], v[u].y, acc.y);
+            acc.z = fmaf(e[u], v[u].z, acc.z);
+            acc.w = fmaf(e[u], v[u].w, acc.w);
+          }
+        }
       }
     }
   } else {

@@ -57,49 +57,23 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, uint32_t 
   __syncthreads();
 }
 
-constexpr int kSelBins1 = 8192;  // key bits [31:19]
-constexpr int kSelShift1 = 19;
-constexpr int kSelShift2 = 9;    // key bits [18:9]
-constexpr int kSelBins2 = 1024;
-constexpr int kSelBins3 = 512;   // key bits [8:0]
-
-// With `hist` holding the histogram of key >> kSelShift1 over the items that
-// take part, find the exact k-th largest key T and how many of the keys equal
-// to T belong to the top k (the rest of the top k is every key above T).
-// key_of(i) gives item i's key and valid(i) whether it takes part; two more
-// histograms touch only the items still in play.  `sh` holds 3 scratch words.
-template <class KeyFn, class ValidFn>
-__device__ __forceinline__ void refine_threshold(KeyFn key_of, ValidFn valid, int n, uint32_t k,
-                                                 uint32_t* hist, uint32_t* scratch,
-                                                 uint32_t* sh, uint32_t& T, uint32_t& k_rem) {
-  const int tid = threadIdx.x;
-  find_bin(hist, kSelBins1, k, scratch, sh);
-  const uint32_t b1 = sh[0];
-  k_rem = sh[1];
-  for (int b = tid; b < kSelBins2; b += kSelThreads) hist[b] = 0;
-  __syncthreads();
-  for (int i = tid; i < n; i += kSelThreads) {
-    if (!valid(i)) continue;
-    const uint32_t key = key_of(i);
-    if ((key >> kSelShift1) == b1)
-      atomicAdd(hist + ((key >> kSelShift2) & (kSelBins2 - 1)), 1u);
-  }
-  __syncthreads();
-  find_bin(hist, kSelBins2, k_rem, scratch, sh);
-  const uint32_t pre2 = (b1 << (kSelShift1 - kSelShift2)) | sh[0];
-  k_rem = sh[1];
-  for (int b = tid; b < kSelBins3; b += kSelThreads) hist[b] = 0;
-  __syncthreads();
-  for (int i = tid; i < n; i += kSelThreads) {
-    if (!valid(i)) continue;
-    const uint32_t key = key_of(i);
-    if ((key >> kSelShift2) == pre2) atomicAdd(hist + (key & (kSelBins3 - 1)), 1u);
-  }
-  __syncthreads();
-  find_bin(hist, kSelBins3, k_rem, scratch, sh);
-  T = (pre2 << kSelShift2) | sh[0];
-  k_rem = sh[1];
-  __syncthreads();
+// Bins of a key range [rlo, rhi] (inclusive): bin(key) = (key - rlo) >>
+// shift, with shift the bits of (rhi - rlo) beyond nbits, so that the range
+// splits into at most 2^nbits bins of 2^shift keys.
+DSA_DEV int range_shift(uint32_t rlo, uint32_t rhi, int nbits) {
+  const uint32_t wdt = rhi - rlo;
+  const int len = wdt == 0u ? 0 : 32 - __clz(wdt);
+  return len > nbits ? len - nbits : 0;
 }
+// the keys of bin b of [rlo, rhi] (the last bin may be short)
+DSA_DEV void bin_range(uint32_t rlo, uint32_t rhi, int shift, uint32_t b, uint32_t* blo,
+                       uint32_t* bhi) {
+  const uint64_t l = static_cast<uint64_t>(rlo) + (static_cast<uint64_t>(b) << shift);
+  const uint64_t h = l + (1ull << shift) - 1ull;
+  *blo = static_cast<uint32_t>(l);
+  *bhi = h < rhi ? static_cast<uint32_t>(h) : rhi;
+}
+
+constexpr int kSelBins1 = 8192;  // histogram bins of one selection round
 
 }  // namespace dsa

@@ -844,23 +844,6 @@ __device__ void block_find_bin(const uint32_t* hist, int nb, uint32_t k_rem, uin
   }
 }
 
-// Bins of a key range [rlo, rhi] (inclusive): bin(key) = (key - rlo) >>
-// shift, with shift the bits of (rhi - rlo) beyond nbits, so that the range
-// splits into at most 2^nbits bins of 2^shift keys.
-__device__ __forceinline__ int range_shift(uint32_t rlo, uint32_t rhi, int nbits) {
-  const uint32_t wdt = rhi - rlo;
-  const int len = wdt == 0u ? 0 : 32 - __clz(wdt);
-  return len > nbits ? len - nbits : 0;
-}
-// the keys of bin b of [rlo, rhi] (the last bin may be short)
-__device__ __forceinline__ void bin_range(uint32_t rlo, uint32_t rhi, int shift, uint32_t b,
-                                          uint32_t* blo, uint32_t* bhi) {
-  const uint64_t l = static_cast<uint64_t>(rlo) + (static_cast<uint64_t>(b) << shift);
-  const uint64_t h = l + (1ull << shift) - 1ull;
-  *blo = static_cast<uint32_t>(l);
-  *bhi = h < rhi ? static_cast<uint32_t>(h) : rhi;
-}
-
 // A score row: its valid count and where it lives.
 struct RowRef {
   const float* src;
