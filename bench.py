@@ -559,7 +559,7 @@ def run_product(args):
         cpu = cpu_baseline(wl, args.cpu_seconds)
 
     if rank == 0:
-        launches_per_step = 3 + (1 if lay.num_parts > 1 else 0) + (1 if sharded else 0)
+        launches_per_step = int(lay.launches)  # the library's own count for this layout
         cfg = describe(wl)
         cfg["parallelism"] = f"dp{world} (independent request batches per GPU)"
         cfg["l2"] = ("flushed between timed steps (512 MB write, then 256 MB read); "

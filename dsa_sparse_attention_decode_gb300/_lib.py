@@ -96,6 +96,8 @@ class DsaDecodeLayout(ctypes.Structure):
         ("part_lse", c_int64),
         ("num_splits", c_int32),
         ("num_parts", c_int32),
+        ("launches", c_int32),
+        ("reserved", c_int32),
         ("total_bytes", c_int64),
     ]
 
@@ -105,6 +107,7 @@ PROTOTYPES = {
     "dsa_abi_version": (c_int, []),
     "dsa_status_string": (c_char_p, [c_int]),
     "dsa_read_error": (c_int, [c_void_p, POINTER(c_int32), c_void_p]),
+    "dsa_selftest_bounded_wait": (c_int, [c_int32, c_void_p, c_void_p, c_void_p]),
     "dsa_indexer_scores": (c_int, [c_void_p, c_void_p, POINTER(DsaPagedCache), POINTER(DsaRows),
                                    c_int32, c_int32, c_void_p, c_int64, c_void_p, c_void_p]),
     "dsa_topk_workspace_size": (c_size_t, [c_int32, c_int64]),

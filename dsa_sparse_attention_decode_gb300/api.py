@@ -97,6 +97,14 @@ def dsa_read_error(d_err: torch.Tensor, stream=None) -> int:
     return int(h.value)
 
 
+def dsa_selftest_bounded_wait(limit_us: int, d_err, d_waited_ns, stream=None):
+    """The library's bounded on-chip wait on a phase nothing completes (see
+    the header): sets DSA_DEVERR_TIMEOUT in d_err and the time waited (ns) in
+    d_waited_ns (a one-element int64 tensor)."""
+    _check(C.lib().dsa_selftest_bounded_wait(int(limit_us), _ptr(d_err), _ptr(d_waited_ns),
+                                             _stream(stream)), "dsa_selftest_bounded_wait")
+
+
 def dsa_indexer_scores(q_idx, w_idx, idx_k: PagedCache, rows: Rows, scores, d_err,
                        shard: int = 0, num_shards: int = 1, stream=None):
     c, r = idx_k.c(), rows.c()

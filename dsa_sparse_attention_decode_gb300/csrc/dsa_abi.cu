@@ -138,9 +138,11 @@ cudaError_t make_kv_fp8_tmap(CUtensorMap* map, const void* data, int num_pages, 
   cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kKvDim)};
   cuuint32_t box[2] = {128u, 1u};
   cuuint32_t estride[2] = {1u, 1u};
+  // no L2 promotion: a 576-byte row starts 64 bytes off a 128-byte line for
+  // every other row, so wider fetches would read bytes of neighbouring rows
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(data), gdim, gstride,
                    box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -228,6 +230,14 @@ int run_sparse_mla(const uint16_t* q, int32_t heads, float sm_scale, const dsa_p
 extern "C" {
 
 int dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+int dsa_selftest_bounded_wait(int32_t limit_us, int32_t* d_err, uint64_t* d_waited_ns,
+                              void* stream) {
+  if (limit_us < 0 || limit_us > 2000000 || d_err == nullptr || d_waited_ns == nullptr)
+    return DSA_ERR_INVALID_ARG;
+  return cuda_status(launch_bounded_wait_selftest(static_cast<uint64_t>(limit_us) * 1000u, d_err,
+                                                  d_waited_ns, static_cast<cudaStream_t>(stream)));
+}
 
 const char* dsa_status_string(int status) {
   switch (status) {
@@ -510,6 +520,11 @@ int dsa_decode_workspace_layout(const dsa_decode_desc* d, dsa_decode_layout* lay
     L.part_out = L.part_lse = -1;
   }
   L.total_bytes = off;
+  // indexer, top-k (three launches in its segment form), the shard merge,
+  // the attention and the LSE merge of its parts
+  L.launches = 1 + (topk_uses_workspace(static_cast<int>(W * R), L.ld_scores) ? 3 : 1) +
+               (W > 1 ? 1 : 0) + 1 + (L.num_parts > 1 ? 1 : 0);
+  L.reserved = 0;
   if (mla_smem_bytes(static_cast<int>(H), d->kv[0].dtype == DSA_DTYPE_FP8_E4M3,
                      split_chunk(S, static_cast<int>(k))) > 227 * 1024)
     return DSA_ERR_UNSUPPORTED;

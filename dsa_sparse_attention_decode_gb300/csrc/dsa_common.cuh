@@ -100,16 +100,17 @@ DSA_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 
 // Wait for the phase with the given parity to complete.  Returns false when
-// the CTA-wide abort flag is set or the wait runs past kWaitTimeoutNs (it then
-// sets the flag itself).  Never spins forever.
-DSA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// the CTA-wide abort flag is set or the wait runs past limit_ns (the kernels
+// use kWaitTimeoutNs; it then sets the flag itself).  Never spins forever.
+DSA_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                       uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         return false;
       }

@@ -177,6 +177,12 @@ cudaError_t launch_lse_merge(const float* O_parts, const float* lse_parts, int p
                              cudaStream_t stream, bool pdl = false,
                              const float* max_parts = nullptr, float* out_max = nullptr);
 
+// one CTA that waits on an mbarrier phase nothing completes, with the
+// kernels' bounded wait and the given limit; sets DSA_DEVERR_TIMEOUT in d_err
+// and the time it waited (ns) in *waited_ns
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, int32_t* d_err, uint64_t* waited_ns,
+                                         cudaStream_t stream);
+
 int num_sms();
 
 }  // namespace dsa

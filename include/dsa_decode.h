@@ -166,6 +166,20 @@ const char* dsa_status_string(int status);
 int dsa_read_error(const int32_t* d_err, int32_t* h_err, void* stream);
 
 /*
+ * dsa_selftest_bounded_wait -- run, in one CTA with nothing else in flight,
+ * the bounded on-chip wait every kernel of this library uses (DSpark page,
+ * fail-closed convention: a wait that cannot complete ends in a reported
+ * error, not a hang) on an mbarrier phase that nothing completes, giving up
+ * after limit_us microseconds (0 .. 2000000; the kernels use 2 s).
+ *   d_err:       device int32, OR-ed with DSA_DEVERR_TIMEOUT when the wait
+ *                gives up (it always does)
+ *   d_waited_ns: device uint64, the time the wait took (ns of %globaltimer)
+ * Errors: DSA_ERR_INVALID_ARG for a bad limit or NULL pointers.
+ */
+int dsa_selftest_bounded_wait(int32_t limit_us, int32_t* d_err, uint64_t* d_waited_ns,
+                              void* stream);
+
+/*
  * dsa_indexer_scores -- DSA indexer over one (shard of a) paged index-K
  * cache.  DCP page, Motivation (score the whole sequence before selecting)
  * and Modifications / Indexer decode (each shard scores its own index-K
@@ -466,6 +480,8 @@ typedef struct {
   int64_t part_out, part_lse;
   int32_t num_splits;
   int32_t num_parts;
+  int32_t launches;  /* kernels one dsa_decode call launches with this layout */
+  int32_t reserved;
   int64_t total_bytes;
 } dsa_decode_layout;
 

@@ -151,3 +151,9 @@ def test_decode_workspace_layout_host_only(lib):
     # a workspace that is too small is refused before any launch
     assert lib.dsa_decode(ctypes.byref(d), ctypes.c_void_p(256), lay.total_bytes - 1,
                           ctypes.c_void_p(16), None) == C.DSA_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_selftest_bounded_wait_rejects_bad_limits(lib):
+    assert lib.dsa_selftest_bounded_wait(-1, ctypes.c_void_p(16), ctypes.c_void_p(16), None) == C.DSA_ERR_INVALID_ARG
+    assert lib.dsa_selftest_bounded_wait(3_000_000, ctypes.c_void_p(16), ctypes.c_void_p(16), None) == C.DSA_ERR_INVALID_ARG
+    assert lib.dsa_selftest_bounded_wait(10, None, ctypes.c_void_p(16), None) == C.DSA_ERR_INVALID_ARG

@@ -457,3 +457,19 @@ def test_long_single_row_max_length():
     run = DecodeRun(dw)
     assert run.run() == 0
     check_decode_rows(run, [0])
+
+
+@pytest.mark.parametrize("limit_us", [0, 1000, 20000])
+def test_bounded_wait_gives_up_and_reports(limit_us):
+    """The kernels' bounded mbarrier wait, on a phase nothing completes: it
+    returns after its limit (not before, and within a few ms after), sets
+    DSA_DEVERR_TIMEOUT in the error word, and the context stays usable."""
+    err = _err()
+    waited = torch.zeros(1, dtype=torch.int64, device=DEV)
+    api.dsa_selftest_bounded_wait(limit_us, err, waited)
+    assert api.dsa_read_error(err) & C.DSA_DEVERR_TIMEOUT
+    w_ns = int(waited.item())
+    assert limit_us * 1000 <= w_ns <= limit_us * 1000 + 5_000_000
+    # the device still runs work after the timeout
+    x = torch.arange(1000, device=DEV)
+    assert int(x.sum().item()) == 999 * 1000 // 2
