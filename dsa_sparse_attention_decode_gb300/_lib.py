@@ -114,7 +114,7 @@ PROTOTYPES = {
     "dsa_topk": (c_int, [c_void_p, c_int64, c_void_p, c_int32, c_int32, c_int32, c_int32,
                          c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
     "dsa_shard_topk_merge": (c_int, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
-                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+                                     c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "dsa_sparse_mla_decode_workspace_size": (c_size_t, [c_int32, c_int32, c_int32, c_int32]),
     "dsa_sparse_mla_decode": (c_int, [c_void_p, c_int32, c_float, POINTER(DsaPagedCache),
                                       POINTER(DsaRows), c_void_p, c_void_p, c_int32, c_int32,

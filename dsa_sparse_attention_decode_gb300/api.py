@@ -142,10 +142,10 @@ def dsa_cache_write(kv_in, tok_req, tok_pos, num_reqs: int, kv: Sequence[PagedCa
 
 
 def dsa_shard_topk_merge(cand_score, cand_pos, cand_count, out_idx, out_count, owned_local,
-                         owned_count, d_err, stream=None):
+                         owned_count, d_err, pos_bound: int = 0, stream=None):
     W, R, k = (int(x) for x in cand_score.shape)
     _check(C.lib().dsa_shard_topk_merge(_ptr(cand_score), _ptr(cand_pos), _ptr(cand_count), W, R,
-                                        k, _ptr(out_idx), _ptr(out_count), _ptr(owned_local),
+                                        k, int(pos_bound), _ptr(out_idx), _ptr(out_count), _ptr(owned_local),
                                         _ptr(owned_count), _ptr(d_err), _stream(stream)),
            "dsa_shard_topk_merge")
 

@@ -347,10 +347,11 @@ int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* valid_len, i
 
 int dsa_shard_topk_merge(const float* cand_score, const int32_t* cand_pos,
                          const int32_t* cand_count, int32_t num_shards, int32_t num_rows,
-                         int32_t k, int32_t* out_idx, int32_t* out_count, int32_t* owned_local,
-                         int32_t* owned_count, int32_t* d_err, void* stream) {
+                         int32_t k, int32_t pos_bound, int32_t* out_idx, int32_t* out_count,
+                         int32_t* owned_local, int32_t* owned_count, int32_t* d_err,
+                         void* stream) {
   if (num_shards < 1 || num_shards > kMaxShards || num_rows < 0 || k < 1 || k > 4096 ||
-      d_err == nullptr)
+      pos_bound < 0 || d_err == nullptr)
     return DSA_ERR_INVALID_ARG;
   if (merge_smem_bytes(num_shards, k) > 227 * 1024) return DSA_ERR_UNSUPPORTED;
   if (num_rows == 0) return DSA_OK;
@@ -358,7 +359,7 @@ int dsa_shard_topk_merge(const float* cand_score, const int32_t* cand_pos,
       !owned_count)
     return DSA_ERR_INVALID_ARG;
   MergeTopkLaunch L{cand_score, cand_pos, cand_count, num_shards, num_rows, k,
-                    out_idx,    out_count, owned_local, owned_count, d_err};
+                    out_idx,    out_count, owned_local, owned_count, d_err, pos_bound};
   return cuda_status(launch_shard_topk_merge(L, static_cast<cudaStream_t>(stream)));
 }
 
@@ -631,7 +632,8 @@ int dsa_decode(const dsa_decode_desc* d, void* workspace, size_t workspace_bytes
                       topk_cnt,
                       reinterpret_cast<int32_t*>(ws + lay.owned_local),
                       reinterpret_cast<int32_t*>(ws + lay.owned_count),
-                      d_err};
+                      d_err,
+                      d->rows.max_len};
     if (launch_shard_topk_merge(L, s, true) != cudaSuccess) return DSA_ERR_CUDA;
   }
   // 4. sparse MLA over each shard's owned rows, split-K

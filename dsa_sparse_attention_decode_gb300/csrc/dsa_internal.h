@@ -99,7 +99,11 @@ struct MergeTopkLaunch {
   int32_t* owned_local;
   int32_t* owned_count;
   int32_t* d_err;
+  int32_t pos_bound;  // every candidate position is below it (0: unknown)
 };
+// With a position bound whose bitmaps fit in shared memory the merge marks the
+// selection in a bitmap of global positions; otherwise it ranks candidates by
+// binary searches in the other lists.
 cudaError_t launch_shard_topk_merge(const MergeTopkLaunch& p, cudaStream_t stream,
                                    bool pdl = false);
 

@@ -237,6 +237,252 @@ __global__ void __launch_bounds__(kMergeThreads, 1) shard_topk_merge_kernel(cons
   if (tid == 0) P.out_count[r] = static_cast<int>(out_cnt);
 }
 
+// ------------------------------------------------------------ top-k merge,
+// bitmap form
+//
+// With every candidate position below a known bound: the same exact
+// threshold T, then the selection is marked in two bitmaps over the row's
+// global positions (above T; equal to T).  Walking the bitmap words in
+// position order takes the ties lowest positions first and gives every
+// selected position its slot in the global list; a shard's owned list is the
+// same walk restricted to the bits p with p % W == w.  No search per
+// candidate, and both lists come out in ascending order.
+constexpr int kMaxBitmapWords = 8192;  // positions below 262144
+
+struct MergeBmSmem {
+  int nw, off_keys, off_pos, off_hist, off_gt, off_eq, off_misc, total;
+};
+
+__host__ __device__ inline MergeBmSmem merge_bm_smem(int W, int k, int pos_bound) {
+  MergeBmSmem m{};
+  const int N = W * k;
+  m.nw = ((pos_bound + 31) / 32 + 3) / 4 * 4;
+  m.off_keys = 0;
+  m.off_pos = N * 4;
+  m.off_hist = 2 * N * 4;
+  m.off_gt = m.off_hist + kSelBins1 * 4;
+  m.off_eq = m.off_gt + m.nw * 4;
+  m.off_misc = m.off_eq + m.nw * 4;
+  m.total = m.off_misc + 1024;
+  return m;
+}
+
+// exclusive prefix sum of v over the 1024 threads; *total gets the sum
+__device__ __forceinline__ uint32_t excl_scan1024(uint32_t v, uint32_t* scratch, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  __syncthreads();  // scratch is free
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  const uint32_t wt = scratch[lane];
+  uint32_t winc = wt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, winc, o);
+    if (lane >= o) winc += t;
+  }
+  *total = __shfl_sync(0xffffffffu, winc, 31);
+  return __shfl_sync(0xffffffffu, winc - wt, warp) + incl - v;
+}
+
+__global__ void __launch_bounds__(kMergeThreads, 1)
+    shard_merge_bitmap_kernel(const MergeTopkLaunch P, const MergeBmSmem S) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int W = P.W, k = P.k, R = P.rows, N = W * k;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + S.off_keys);
+  int* pos = reinterpret_cast<int*>(smem + S.off_pos);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + S.off_hist);
+  uint32_t* gtb = reinterpret_cast<uint32_t*>(smem + S.off_gt);
+  uint32_t* eqb = reinterpret_cast<uint32_t*>(smem + S.off_eq);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + S.off_misc);
+  uint32_t* scratch = misc;                      // 32
+  uint32_t* sh = misc + 32;                      // 8
+  int* cnt = reinterpret_cast<int*>(misc + 64);  // [8]
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int bound = P.pos_bound;
+  pdl_trigger();
+  pdl_wait();  // the candidate lists come from the previous grid
+
+  if (tid < W) {
+    int c = __ldcg(P.cand_count + tid * R + r);
+    if (c < 0 || c > k) {
+      raise_err(P.d_err, DSA_DEVERR_INDEX);
+      c = c < 0 ? 0 : k;
+    }
+    cnt[tid] = c;
+  }
+  for (int j = tid; j < S.nw; j += kMergeThreads) {
+    gtb[j] = 0u;
+    eqb[j] = 0u;
+  }
+  __syncthreads();
+  int total = 0;
+  for (int v = 0; v < W; ++v) total += cnt[v];
+  const bool all = total <= k;
+  auto valid = [&](int e) { return (e % k) < cnt[e / k] && pos[e] >= 0; };
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  {
+    constexpr int kU = 8;  // loads in flight per thread
+    for (int e0 = 0; e0 < N; e0 += kMergeThreads * kU) {
+      uint32_t key[kU];
+      int pv[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int e = e0 + u * kMergeThreads + tid;
+        const int w = e / k, i = e - w * k;
+        pv[u] = -2;
+        if (e < N && i < cnt[w]) {
+          const long long g = (static_cast<long long>(w) * R + r) * k + i;
+          key[u] = score_key(__ldcg(P.cand_score + g));
+          pv[u] = __ldcg(P.cand_pos + g);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int e = e0 + u * kMergeThreads + tid;
+        if (e >= N) continue;
+        if (pv[u] == -2) {
+          pos[e] = -1;
+          continue;
+        }
+        const int w = e / k;
+        int p = pv[u];
+        if (p < 0 || p >= bound || p % W != w) {
+          raise_err(P.d_err, DSA_DEVERR_INDEX);
+          p = -1;  // left out
+        }
+        keys[e] = key[u];
+        pos[e] = p;
+        if (p >= 0) {
+          kmin = min(kmin, key[u]);
+          kmax = max(kmax, key[u]);
+        }
+      }
+    }
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if ((tid & 31) == 0) {
+    scratch[warp] = kmin;
+    hist[warp] = kmax;  // the histogram is not in use yet
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t a = __reduce_min_sync(0xffffffffu, scratch[tid]);
+    const uint32_t b = __reduce_max_sync(0xffffffffu, hist[tid]);
+    if (tid == 0) {
+      sh[4] = a;
+      sh[5] = b;
+    }
+  }
+  __syncthreads();
+  uint32_t T = 0, k_rem = static_cast<uint32_t>(k);
+  if (!all) {
+    uint32_t rlo = sh[4], rhi = sh[5];
+    __syncthreads();  // sh is read before find_bin writes it
+    while (rlo < rhi) {
+      const int shift = range_shift(rlo, rhi, 13);
+      for (int b = tid; b < kSelBins1; b += kMergeThreads) hist[b] = 0;
+      __syncthreads();
+      for (int e = tid; e < N; e += kMergeThreads) {
+        if (!valid(e)) continue;
+        const uint32_t key = keys[e];
+        if (key >= rlo && key <= rhi) atomicAdd(hist + ((key - rlo) >> shift), 1u);
+      }
+      __syncthreads();
+      find_bin(hist, kSelBins1, k_rem, scratch, sh);  // ends with a barrier
+      bin_range(rlo, rhi, shift, sh[0], &rlo, &rhi);
+      k_rem = sh[1];
+      __syncthreads();  // sh and hist are read before the next round writes them
+    }
+    T = rlo;
+  }
+  // the selection in the bitmaps: above T for sure; ties at T taken later
+  for (int e = tid; e < N; e += kMergeThreads) {
+    if (!valid(e)) continue;
+    const uint32_t key = keys[e];
+    const int p = pos[e];
+    if (all || key > T) atomicOr(gtb + (p >> 5), 1u << (p & 31));
+    else if (key == T) atomicOr(eqb + (p >> 5), 1u << (p & 31));
+  }
+  __syncthreads();
+  // walk the words in position order: thread t a contiguous run of words
+  const int nwu = (bound + 31) >> 5;
+  const int per = (nwu + kMergeThreads - 1) / kMergeThreads;
+  const int j0 = min(nwu, tid * per), j1 = min(nwu, j0 + per);
+  uint32_t e_mine = 0;
+  for (int j = j0; j < j1; ++j) e_mine += __popc(eqb[j]);
+  uint32_t e_tot;
+  uint32_t eq_before = excl_scan1024(e_mine, scratch, &e_tot);
+  for (int j = j0; j < j1; ++j) {
+    uint32_t ew = eqb[j];
+    const uint32_t room = eq_before < k_rem ? k_rem - eq_before : 0u;
+    const uint32_t pe = __popc(ew);
+    if (pe > room) {  // keep the lowest `room` ties of the word
+      uint32_t keep = 0u;
+      for (uint32_t t = 0; t < room; ++t) {
+        const uint32_t bit = ew & (0u - ew);
+        keep |= bit;
+        ew ^= bit;
+      }
+      ew = keep;
+    }
+    eq_before += pe;
+    gtb[j] |= ew;  // the final selection (this thread's words only)
+  }
+  // global list
+  uint32_t s_mine = 0;
+  for (int j = j0; j < j1; ++j) s_mine += __popc(gtb[j]);
+  uint32_t s_tot;
+  uint32_t slot = excl_scan1024(s_mine, scratch, &s_tot);
+  int32_t* oidx = P.out_idx + static_cast<long long>(r) * k;
+  for (int j = j0; j < j1; ++j) {
+    uint32_t sel = gtb[j];
+    while (sel != 0u) {
+      const int b = __ffs(sel) - 1;
+      sel &= sel - 1u;
+      if (slot < static_cast<uint32_t>(k)) oidx[slot] = j * 32 + b;
+      ++slot;
+    }
+  }
+  const uint32_t out_cnt = min(s_tot, static_cast<uint32_t>(k));
+  for (int j = static_cast<int>(out_cnt) + tid; j < k; j += kMergeThreads) oidx[j] = -1;
+  if (tid == 0) P.out_count[r] = static_cast<int>(out_cnt);
+  // every shard's owned list: the bits p of word j with p % W == w
+  for (int w = 0; w < W; ++w) {
+    auto mask_of = [&](int j) {
+      // bits b with (32 j + b) % W == w: the first is b0, then every W-th
+      const int b0 = ((w - (32 * j) % W) % W + W) % W;
+      uint32_t m = 0u;
+      for (int b = b0; b < 32; b += W) m |= 1u << b;
+      return m;
+    };
+    uint32_t o_mine = 0;
+    for (int j = j0; j < j1; ++j) o_mine += __popc(gtb[j] & mask_of(j));
+    uint32_t o_tot;
+    uint32_t os = excl_scan1024(o_mine, scratch, &o_tot);
+    int32_t* ol = P.owned_local + (static_cast<long long>(w) * R + r) * k;
+    for (int j = j0; j < j1; ++j) {
+      uint32_t sel = gtb[j] & mask_of(j);
+      while (sel != 0u) {
+        const int b = __ffs(sel) - 1;
+        sel &= sel - 1u;
+        if (os < static_cast<uint32_t>(k)) ol[os] = (j * 32 + b) / W;
+        ++os;
+      }
+    }
+    const uint32_t oc = min(o_tot, static_cast<uint32_t>(k));
+    for (int j = static_cast<int>(oc) + tid; j < k; j += kMergeThreads) ol[j] = -1;
+    if (tid == 0) P.owned_count[w * R + r] = static_cast<int>(oc);
+  }
+}
+
 // ------------------------------------------------------------ LSE merge
 //
 // lse = ln sum_p exp(lse_p), out = sum_p exp(lse_p - lse) O_p; parts whose
@@ -426,6 +672,16 @@ int merge_smem_bytes(int W, int k) { return merge_smem(W, k).total; }
 
 cudaError_t launch_shard_topk_merge(const MergeTopkLaunch& p, cudaStream_t stream, bool pdl) {
   if (p.rows == 0) return cudaSuccess;
+  if (p.pos_bound > 0 && (p.pos_bound + 31) / 32 <= kMaxBitmapWords) {
+    const MergeBmSmem S = merge_bm_smem(p.W, p.k, p.pos_bound);
+    if (S.total <= 227 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(shard_merge_bitmap_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, S.total);
+      if (e != cudaSuccess) return e;
+      return launch_ex(shard_merge_bitmap_kernel, dim3(p.rows), dim3(kMergeThreads), S.total,
+                       stream, pdl, p, S);
+    }
+  }
   const int smem = merge_smem_bytes(p.W, p.k);
   cudaError_t e = cudaFuncSetAttribute(shard_topk_merge_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

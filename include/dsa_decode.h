@@ -68,7 +68,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 2
+#define DSA_ABI_VERSION 3
 
 /* fixed geometry */
 #define DSA_INDEX_HEADS 64   /* indexer heads per query row */
@@ -257,6 +257,12 @@ int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* valid_len,
  *   cand_pos:   device int32 [W][num_rows][k] global positions (ascending in
  *               each list); shard w's positions are == w mod W
  *   cand_count: device int32 [W][num_rows]
+ *   pos_bound:  0, or a bound every candidate position is below (the
+ *               requests' longest length); with one of at most 262144 the
+ *               merge marks the selection in a bitmap of positions instead
+ *               of ranking every candidate by searches in the other lists
+ *               (same result; a position at or above the bound sets
+ *               DSA_DEVERR_INDEX and is left out)
  *   out_idx:    device int32 [num_rows][k] global top-k of the union (ties at
  *               the k-th place to the lower position), ascending, -1 pad
  *   out_count:  device int32 [num_rows] = min(k, sum_w cand_count)
@@ -266,7 +272,7 @@ int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* valid_len,
  */
 int dsa_shard_topk_merge(const float* cand_score, const int32_t* cand_pos,
                          const int32_t* cand_count, int32_t num_shards,
-                         int32_t num_rows, int32_t k, int32_t* out_idx,
+                         int32_t num_rows, int32_t k, int32_t pos_bound, int32_t* out_idx,
                          int32_t* out_count, int32_t* owned_local,
                          int32_t* owned_count, int32_t* d_err, void* stream);
 

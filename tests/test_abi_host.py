@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert lib.dsa_abi_version() == 2
+    assert lib.dsa_abi_version() == 3
     for s in range(7):
         assert lib.dsa_status_string(s).startswith(b"DSA_")
     assert lib.dsa_status_string(99) == b"unknown dsa status"

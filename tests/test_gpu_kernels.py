@@ -187,16 +187,27 @@ def test_topk_nan_flag():
     assert api.dsa_read_error(err) & C.DSA_DEVERR_NAN
 
 
-def test_shard_merge_against_oracle():
+@pytest.mark.parametrize("W,k,n,levels,bounded", [
+    (3, 256, 2000, 50, False), (3, 256, 2000, 50, True),         # many ties at the k-th place
+    (4, 2048, 40000, 1 << 30, False), (4, 2048, 40000, 1 << 30, True),
+    (8, 2048, 9000, 7, True),                                     # few distinct scores, 8 shards
+    (2, 2048, 3000, 1 << 30, True),                               # short rows: the union < k
+    (5, 512, 262144, 1000, True),                                 # the largest bitmap
+])
+def test_shard_merge_against_oracle(W, k, n, levels, bounded):
+    """Both forms of the merge (bitmap over positions when a position bound
+    is given, ranking searches otherwise) against the oracle's merge."""
     rng = np.random.default_rng(2)
-    W, R, k, n = 3, 4, 256, 2000
+    R = 4
     cs = np.zeros((W, R, k), np.float32)
     cp = np.full((W, R, k), -1, np.int32)
     cc = np.zeros((W, R), np.int32)
-    s_full = rng.integers(0, 50, (R, n)).astype(np.float32)
+    s_full = rng.integers(0, levels, (R, n)).astype(np.float32)
+    if levels > 1000:
+        s_full = rng.standard_normal((R, n)).astype(np.float32)
     for r in range(R):
         for w in range(W):
-            pos = np.arange(w, n - r * 300, W)
+            pos = np.arange(w, n - r * (n // 7), W)
             j = orc.topk_select(s_full[r, pos].astype(np.float64), k)
             cc[w, r] = len(j)
             cs[w, r, : len(j)] = s_full[r, pos[j]]
@@ -207,7 +218,8 @@ def test_shard_merge_against_oracle():
     ol = torch.zeros((W, R, k), dtype=torch.int32, device=DEV)
     ocnt = torch.zeros((W, R), dtype=torch.int32, device=DEV)
     err = _err()
-    api.dsa_shard_topk_merge(t(cs), t(cp), t(cc), oi, oc, ol, ocnt, err)
+    api.dsa_shard_topk_merge(t(cs), t(cp), t(cc), oi, oc, ol, ocnt, err,
+                             pos_bound=n if bounded else 0)
     assert api.dsa_read_error(err) == 0
     for r in range(R):
         sel, owned = orc.merge_candidates([cs[w, r, : cc[w, r]] for w in range(W)],
