@@ -261,6 +261,48 @@ def test_sparse_mla_alone(cfg):
             assert eo <= (2e-3 if cfg == 1 else 5e-3) and el <= 1e-4, (S, r, eo, el)
 
 
+def test_sparse_mla_many_rows_split_forms_agree():
+    """420 rows on an fp8 cache with selections of every size from 0 to 2048:
+    the automatic split choice (one split per row here: the output written
+    in place) against four splits merged by their LSEs, every row, and
+    sampled rows against the oracle."""
+    wl = make_workload(config_spec(2, B=70, L_lo=2500, L_hi=4000))
+    dw = upload(wl, DEV)
+    rng = np.random.default_rng(17)
+    k = 2048
+    sizes = [2048, 0, 1, 127, 128, 129, 700, 2047, 64, 2048, 1500, 3]
+    idx = np.full((wl.R, k), -1, np.int32)
+    cnt = np.zeros(wl.R, np.int32)
+    for r in range(wl.R):
+        n = min(sizes[r % len(sizes)], int(wl.row_pos[r]) + 1)
+        idx[r, :n] = rng.choice(int(wl.row_pos[r]) + 1, n, replace=False)
+        cnt[r] = n
+    t = lambda a: torch.from_numpy(a).to(DEV)  # noqa: E731
+    res = {}
+    for S in (0, 4):
+        out = torch.full((wl.R, wl.H, 512), float("nan"), device=DEV)
+        lse = torch.full((wl.R, wl.H), float("nan"), device=DEV)
+        ws = torch.zeros(max(1, api.dsa_sparse_mla_decode_workspace_size(wl.R, wl.H, k, S)),
+                         dtype=torch.uint8, device=DEV)
+        err = _err()
+        api.dsa_sparse_mla_decode(dw.q, wl.sm_scale, dw.kv, dw.rows, t(idx), t(cnt), out, lse,
+                                  err, workspace=ws, num_splits=S)
+        assert api.dsa_read_error(err) == 0
+        res[S] = (out.cpu().numpy(), lse.cpu().numpy())
+    (o0, l0), (o4, l4) = res[0], res[4]
+    assert np.isfinite(o0).all()
+    both_inf = np.isneginf(l0) & np.isneginf(l4)
+    assert np.array_equal(np.isneginf(l0), np.isneginf(l4))
+    assert np.all(np.where(both_inf, 0.0, np.abs(l0 - l4)) <= 1e-4)
+    den = np.abs(o4).max(axis=-1)
+    rel = np.abs(o0 - o4).max(axis=-1) / np.where(den > 0, den, 1.0)
+    assert rel.max() <= 5e-3
+    for r in list(range(0, 24)) + list(range(wl.R - 12, wl.R)) + list(rng.choice(wl.R, 24)):
+        O_ref, l_ref = orc.row_attention(wl, r, idx[r, : cnt[r]])
+        eo, el = attn_err(o0[r], l0[r], O_ref, l_ref)
+        assert eo <= 5e-3 and el <= 1e-4, (r, int(cnt[r]), eo, el)
+
+
 @pytest.mark.parametrize("cfg", [0, 1, 2])
 def test_sparse_mla_prefill_into(cfg):
     """Sparse attention of a prefill chunk (two requests of 40 query rows at

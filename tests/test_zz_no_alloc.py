@@ -61,13 +61,14 @@ def _compare(wl, dw, idx, cnt, S, calls, tol):
         assert np.all(np.where(both_inf, 0.0, np.abs(l - ref_l)) <= 1e-4)
 
 
-@pytest.mark.parametrize("cfg,tol", [(1, 2e-3), (2, 5e-3)])
-def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(cfg, tol):
-    """bf16 and fp8 caches; full selections, then (after the array holds a
-    full call's partials) other selections whose later splits are empty, so
-    that partials left by the earlier call must not reach the result."""
+@pytest.mark.parametrize("cfg,tol,S", [(1, 2e-3, 4), (2, 5e-3, 4), (2, 5e-3, 0)])
+def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(cfg, tol, S):
+    """bf16 and fp8 caches, four splits and the automatic choice (16 splits
+    for these six rows); full selections, then (after the array holds a full
+    call's partials) other selections whose later splits are empty, so that
+    partials left by the earlier call must not reach the result."""
     wl, dw, idx, cnt = _case(cfg)
-    _compare(wl, dw, idx, cnt, 4, 2, tol)
+    _compare(wl, dw, idx, cnt, S, 2, tol)
     rng = np.random.default_rng(5)
     k = 2048
     idx2 = np.full((wl.R, k), -1, np.int32)
@@ -76,7 +77,7 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(cfg, tol):
         n = [1, 65, 1, 2048, 65, 1][r]
         idx2[r, :n] = np.sort(rng.choice(int(wl.row_pos[r]) + 1, n, replace=False))
         cnt2[r] = n
-    _compare(wl, dw, torch.from_numpy(idx2).to(DEV), torch.from_numpy(cnt2).to(DEV), 4, 2, tol)
+    _compare(wl, dw, torch.from_numpy(idx2).to(DEV), torch.from_numpy(cnt2).to(DEV), S, 2, tol)
 
 
 def test_noalloc_refuses_sizes_beyond_the_array():
