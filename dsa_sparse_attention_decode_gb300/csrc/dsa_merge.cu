@@ -325,45 +325,46 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
   int total = 0;
   for (int v = 0; v < W; ++v) total += cnt[v];
   const bool all = total <= k;
-  auto valid = [&](int e) { return (e % k) < cnt[e / k] && pos[e] >= 0; };
+  // a candidate slot holds a position (>= 0) or -1 (past its list, or left out)
+  auto valid = [&](int e) { return pos[e] >= 0; };
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   {
-    constexpr int kU = 8;  // loads in flight per thread
-    for (int e0 = 0; e0 < N; e0 += kMergeThreads * kU) {
-      uint32_t key[kU];
-      int pv[kU];
+    // two slots of every list per thread and round: up to 16 loads in flight
+    constexpr int kU = 2;
+    for (int i0 = 0; i0 < k; i0 += kMergeThreads * kU) {
+      uint32_t key[kU][DSA_MAX_SHARDS];
+      int pv[kU][DSA_MAX_SHARDS];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int e = e0 + u * kMergeThreads + tid;
-        const int w = e / k, i = e - w * k;
-        pv[u] = -2;
-        if (e < N && i < cnt[w]) {
-          const long long g = (static_cast<long long>(w) * R + r) * k + i;
-          key[u] = score_key(__ldcg(P.cand_score + g));
-          pv[u] = __ldcg(P.cand_pos + g);
-        }
-      }
+      for (int u = 0; u < kU; ++u)
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int e = e0 + u * kMergeThreads + tid;
-        if (e >= N) continue;
-        if (pv[u] == -2) {
-          pos[e] = -1;
-          continue;
+        for (int w = 0; w < DSA_MAX_SHARDS; ++w) {
+          const int i = i0 + u * kMergeThreads + tid;
+          key[u][w] = 0u;
+          pv[u][w] = -1;
+          if (w < W && i < cnt[w]) {
+            const long long g = (static_cast<long long>(w) * R + r) * k + i;
+            key[u][w] = score_key(__ldcg(P.cand_score + g));
+            pv[u][w] = __ldcg(P.cand_pos + g);
+          }
         }
-        const int w = e / k;
-        int p = pv[u];
-        if (p < 0 || p >= bound || p % W != w) {
-          raise_err(P.d_err, DSA_DEVERR_INDEX);
-          p = -1;  // left out
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+#pragma unroll
+        for (int w = 0; w < DSA_MAX_SHARDS; ++w) {
+          const int i = i0 + u * kMergeThreads + tid;
+          if (w >= W || i >= k) continue;
+          int p = pv[u][w];
+          if (i < cnt[w] && (p < 0 || p >= bound || p % W != w)) {
+            raise_err(P.d_err, DSA_DEVERR_INDEX);
+            p = -1;  // left out
+          }
+          keys[w * k + i] = key[u][w];
+          pos[w * k + i] = p;
+          if (p >= 0) {
+            kmin = min(kmin, key[u][w]);
+            kmax = max(kmax, key[u][w]);
+          }
         }
-        keys[e] = key[u];
-        pos[e] = p;
-        if (p >= 0) {
-          kmin = min(kmin, key[u]);
-          kmax = max(kmax, key[u]);
-        }
-      }
     }
   }
   kmin = __reduce_min_sync(0xffffffffu, kmin);
@@ -496,11 +497,15 @@ constexpr int kFastParts = 8;
 // With more partials: every thread loads a share of the parts' LSEs, a
 // block reduction gives their maximum, the live parts (LSE finite) are
 // listed in part order by a block scan with their weights exp(lse_p - m),
-// and the value dims accumulate the live partial outputs, kMergeUnroll
-// loads in flight per thread.  The order of every sum is fixed, so the
-// result does not depend on scheduling.
+// and the value dims accumulate the live partial outputs: kListGroups groups
+// of threads take turns of kMergeUnroll consecutive live parts (that many
+// loads in flight per thread), and group 0 adds the groups' sums in order.
+// The order of every sum is fixed, so the result does not depend on
+// scheduling.
 constexpr int kMaxListParts = 1024;
 constexpr int kMergeUnroll = 8;
+constexpr int kListGroups = 4;          // thread groups of the live-list path
+constexpr int kMaxGroupThreads = 768;   // (groups - 1) * padded dv / 4 it reduces over
 
 // sum (kMax: maximum) of v over the CTA; every thread gets it.  red holds 33
 // words.
@@ -537,7 +542,10 @@ __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
   pdl_trigger();
   pdl_wait();  // the partials come from the previous grid
   const long long stride_p = static_cast<long long>(rows) * heads;
-  const int d4 = threadIdx.x;
+  // groups of dpad threads, one float4 of the value dims per thread; more
+  // than one group (the live-list path) splits the live partials between them
+  const int dpad = ((dv / 4 + 31) / 32) * 32;
+  const int d4 = threadIdx.x % dpad, grp = threadIdx.x / dpad, ngrp = blockDim.x / dpad;
   const bool has_d = d4 < dv / 4;
   const float kNegInf = -__int_as_float(0x7f800000);
   float m = kNegInf, den = 0.0f;
@@ -614,7 +622,7 @@ __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
       den = block_reduce<false>(dsum, red);  // its barriers publish live
       const int nl = nlive_s;
       if (has_d) {
-        for (int i0 = 0; i0 < nl; i0 += kMergeUnroll) {
+        for (int i0 = grp * kMergeUnroll; i0 < nl; i0 += ngrp * kMergeUnroll) {
           float4 v[kMergeUnroll];
           float e[kMergeUnroll];
 #pragma unroll
@@ -633,6 +641,19 @@ __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
           }
         }
       }
+    }
+    if (ngrp > 1) {  // the groups' sums: group 0 adds the others
+      __shared__ float4 gacc[kMaxGroupThreads];
+      if (grp > 0 && has_d) gacc[threadIdx.x - dpad] = acc;
+      __syncthreads();
+      if (grp == 0 && has_d)
+        for (int g2 = 1; g2 < ngrp; ++g2) {
+          const float4 o = gacc[(g2 - 1) * dpad + d4];
+          acc.x += o.x;
+          acc.y += o.y;
+          acc.z += o.z;
+          acc.w += o.w;
+        }
     }
   } else {
     for (int p = 0; p < parts; ++p) m = fmaxf(m, __ldcg(lse_parts + p * stride_p + rh));
@@ -654,7 +675,7 @@ __global__ void lse_merge_kernel(const float* __restrict__ O_parts,
     }
   }
   const float inv = m == kNegInf ? 0.0f : 1.0f / den;
-  if (has_d)
+  if (has_d && grp == 0)
     reinterpret_cast<float4*>(out + static_cast<long long>(rh) * dv)[d4] =
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   if (threadIdx.x == 0) out_lse[rh] = m == kNegInf ? m : m + logf(den);
@@ -695,7 +716,13 @@ cudaError_t launch_lse_merge(const float* O_parts, const float* lse_parts, int p
                              bool pdl, const float* max_parts, float* out_max) {
   if (rows * heads == 0) return cudaSuccess;
   if (dv % 4 != 0 || dv / 4 > 1024) return cudaErrorInvalidValue;
-  const int threads = ((dv / 4 + 31) / 32) * 32;  // one float4 of the value dims per thread
+  const int dpad = ((dv / 4 + 31) / 32) * 32;  // one float4 of the value dims per thread
+  // the live-list path splits the partials between groups of dpad threads
+  const int groups = (parts > kFastParts && parts <= kMaxListParts &&
+                      (kListGroups - 1) * dpad <= kMaxGroupThreads)
+                         ? kListGroups
+                         : 1;
+  const int threads = dpad * groups;
   if ((max_parts == nullptr) != (out_max == nullptr)) return cudaErrorInvalidValue;
   return launch_ex(lse_merge_kernel, dim3(rows * heads), dim3(threads), 0, stream, pdl, O_parts,
                    lse_parts, parts, rows, heads, dv, out, out_lse, max_parts, out_max);

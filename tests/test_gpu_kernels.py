@@ -426,13 +426,20 @@ def test_sparse_mla_running_max_moves(cfg):
             assert eo <= 2e-3 and el <= 1e-4, (S, r, eo, el)
 
 
-def test_lse_merge_against_oracle():
+@pytest.mark.parametrize("P,dv", [(5, 512), (9, 512), (40, 512), (128, 512), (128, 96),
+                                  (1030, 512)])
+def test_lse_merge_against_oracle(P, dv):
+    """All three forms of the merge: up to 8 parts (every load at once), the
+    live-list form (9..1024 parts, split between thread groups), and the
+    sequential form beyond; many empty parts (LSE -inf) among them."""
     rng = np.random.default_rng(4)
-    P, R, H, dv = 5, 3, 4, 512
+    R, H = 3, 4
     Op = rng.standard_normal((P, R, H, dv)).astype(np.float32)
     lp = (rng.standard_normal((P, R, H)) * 3).astype(np.float32)
     lp[1, 0, :] = -np.inf
     lp[:, 2, 1] = -np.inf  # a fully empty (row, head)
+    if P > 8:
+        lp[rng.random((P, R, H)) < 0.7] = -np.inf  # most parts empty, as split-K leaves them
     out = torch.zeros((R, H, dv), device=DEV)
     ol = torch.zeros((R, H), device=DEV)
     api.dsa_lse_merge(torch.from_numpy(Op).to(DEV), torch.from_numpy(lp).to(DEV), out, ol)
