@@ -711,7 +711,38 @@ def cpu_baseline(wl, seconds: float):
             "sample": f"{rows} query rows of the same workload (rows 0..{min(rows, wl.R) - 1} in "
                       f"order, {toks / rows:.0f} cached tokens per row on average), one after "
                       f"another, full path (indexer over the row's tokens, exact "
-                      f"top-{wl.topk}, MLA) in float64 numpy, {el:.1f} s"}
+                      f"top-{wl.topk}, MLA) in float64 numpy, {el:.1f} s",
+            "single_thread_config0": single_thread_config0()}
+
+
+# The oracle on the tiny workload (configuration 0: one row over 4096 tokens,
+# 16 heads) with one BLAS thread, in a child process (the thread count of
+# numpy's BLAS is fixed when it loads).
+_SINGLE = """
+import sys, time
+sys.path.insert(0, sys.argv[1])
+from oracle import dsa_oracle as orc
+from workloads import config_spec, make_workload
+wl = make_workload(config_spec(0))
+orc.decode_row(wl, 0)
+t0, n = time.perf_counter(), 0
+while n < 2 or time.perf_counter() - t0 < float(sys.argv[2]):
+    orc.decode_row(wl, 0)
+    n += 1
+print(n / (time.perf_counter() - t0))
+"""
+
+
+def single_thread_config0(seconds: float = 3.0):
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", _SINGLE, ROOT, str(seconds)], env=env,
+                           capture_output=True, text=True, timeout=120)
+        value = float(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, not fatal: the GPU line does not depend on it
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
+    return {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "workload": "configuration 0 (one row, L=4096, bf16, 16 heads), one BLAS thread"}
 
 
 def run_reference(args):

@@ -86,3 +86,13 @@ def test_algorithmic_bytes_closed_form():
     assert b["indexer"] == 2 * (L * 256 + 5 * 4) + 2 * (64 * 128 * 2 + 64 * 4)
     assert b["topk"] == 2 * (L * 4 + k * 4 + 4)
     assert b["mla"] == 2 * (L * 1152 + k * 4 + H * 576 * 2 + H * 512 * 4 + H * 4)
+
+
+def test_single_thread_oracle_figure_on_config0():
+    """The CPU baseline also reports the oracle on configuration 0 with one
+    BLAS thread (run in a child process, so that the thread count holds)."""
+    import bench
+
+    d = bench.single_thread_config0(0.3)
+    assert "error" not in d, d
+    assert d["cores"] == 1 and d["value"] > 0 and d["unit"] == bench.UNIT
