@@ -934,6 +934,33 @@ __device__ __forceinline__ void window_range(uint32_t wlo, int wshift, uint32_t 
   if (b == static_cast<uint32_t>(kWBins - 1)) *rhi = 0xFFFFFFFFu;
 }
 
+// One step of the first histogram: this thread's kU quads (loaded by
+// hist_load); returns whether a NaN was seen.
+template <int NT>
+__device__ __forceinline__ void hist_load(const RowRef& R, int base, int q1, uint32_t (*kv)[4],
+                                          uint32_t* ok) {
+#pragma unroll
+  for (int u = 0; u < kU; ++u) {
+    const int qd = base + u * NT + static_cast<int>(threadIdx.x);
+    ok[u] = qd < q1 ? load_quad(R, qd, kv[u]) : 0u;
+  }
+}
+__device__ __forceinline__ bool hist_step(const uint32_t (*kv)[4], const uint32_t* ok,
+                                          uint32_t wlo, int wshift, uint32_t* hist) {
+  bool nan_seen = false;
+#pragma unroll
+  for (int u = 0; u < kU; ++u)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if ((ok[u] >> e) & 1u) {
+        const uint32_t key = kv[u][e];
+        // NaN keys: above 0xFF800000 (+inf) or below 0x007FFFFF (-inf)
+        nan_seen |= key > 0xFF800000u || key < 0x007FFFFFu;
+        atomicAdd(hist + window_bin(key, wlo, wshift), 1u);
+      }
+  return nan_seen;
+}
+
 // First histogram over quads [q0, q1) of the row; returns whether a NaN was seen.
 template <int NT>
 __device__ bool window_hist_pass(const RowRef& R, int q0, int q1, uint32_t wlo, int wshift,
@@ -941,23 +968,65 @@ __device__ bool window_hist_pass(const RowRef& R, int q0, int q1, uint32_t wlo, 
   bool nan_seen = false;
   for (int base = q0; base < q1; base += NT * kU) {
     uint32_t kv[kU][4], ok[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int qd = base + u * NT + static_cast<int>(threadIdx.x);
-      ok[u] = qd < q1 ? load_quad(R, qd, kv[u]) : 0u;
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if ((ok[u] >> e) & 1u) {
-          const uint32_t key = kv[u][e];
-          // NaN keys: above 0xFF800000 (+inf) or below 0x007FFFFF (-inf)
-          nan_seen |= key > 0xFF800000u || key < 0x007FFFFFu;
-          atomicAdd(hist + window_bin(key, wlo, wshift), 1u);
-        }
+    hist_load<NT>(R, base, q1, kv, ok);
+    nan_seen |= hist_step(kv, ok, wlo, wshift, hist);
   }
   return nan_seen;
+}
+
+// One step of the marking pass: this warp's kU runs starting at run s0
+// (loaded by mark_load).
+__device__ __forceinline__ void mark_load(const RowRef& R, int s0, int r1, uint32_t (*kv)[4],
+                                          uint32_t* ok) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int u = 0; u < kU; ++u) ok[u] = s0 + u < r1 ? load_quad(R, (s0 + u) * 32 + lane, kv[u]) : 0u;
+}
+__device__ __forceinline__ void mark_step(const RowRef& R, const uint32_t (*kv)[4],
+                                          const uint32_t* ok, int s0, int r1, uint32_t rlo,
+                                          uint32_t rhi, bool exact, uint32_t* gt_out,
+                                          uint32_t* eq_out, uint32_t* cand_cnt, uint2* cand_out) {
+  const int lane = threadIdx.x & 31;
+  const int nwu = (R.n + 31) >> 5;
+#pragma unroll
+  for (int u = 0; u < kU; ++u) {
+    if (s0 + u >= r1) break;  // warp-uniform
+    uint32_t gn = 0u, en = 0u;  // 4-bit masks: above / inside the range
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const bool v = (ok[u] >> e) & 1u;
+      const uint32_t key = kv[u][e];
+      gn |= (v && key > rhi ? 1u : 0u) << e;
+      en |= (v && key >= rlo && key <= rhi ? 1u : 0u) << e;
+    }
+    const int sh4 = 4 * (lane & 7);
+    uint32_t gw = gn << sh4, ew = en << sh4;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      gw |= __shfl_xor_sync(0xffffffffu, gw, o);
+      ew |= __shfl_xor_sync(0xffffffffu, ew, o);
+    }
+    const int word = (s0 + u) * 4 + (lane >> 3);
+    if ((lane & 7) == 0 && word < nwu) {
+      gt_out[word] = gw;
+      if (exact) eq_out[word] = ew;
+    }
+    if (!exact && __any_sync(0xffffffffu, en != 0u)) {
+      const uint32_t c = __popc(en);
+      const uint32_t incl = warp_incl_scan(c, lane);
+      uint32_t slot = 0;
+      if (lane == 31) slot = atomicAdd(cand_cnt, incl);
+      slot = __shfl_sync(0xffffffffu, slot, 31) + incl - c;
+      const int p0 = ((s0 + u) * 32 + lane) * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if ((en >> e) & 1u) {
+          if (slot < static_cast<uint32_t>(kRCand))
+            cand_out[slot] = make_uint2(kv[u][e], static_cast<uint32_t>(p0 + e));
+          ++slot;
+        }
+    }
+  }
 }
 
 // Marking pass over the runs [r0, r1) of 32 quads (128 positions) of the
@@ -969,51 +1038,11 @@ __device__ bool window_hist_pass(const RowRef& R, int q0, int q1, uint32_t wlo, 
 template <int NT>
 __device__ void mark_pass(const RowRef& R, int r0, int r1, uint32_t rlo, uint32_t rhi, bool exact,
                           uint32_t* gt_out, uint32_t* eq_out, uint32_t* cand_cnt, uint2* cand_out) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwu = (R.n + 31) >> 5;
+  const int warp = threadIdx.x >> 5;
   for (int s0 = r0 + warp * kU; s0 < r1; s0 += (NT / 32) * kU) {
     uint32_t kv[kU][4], ok[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) ok[u] = s0 + u < r1 ? load_quad(R, (s0 + u) * 32 + lane, kv[u]) : 0u;
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (s0 + u >= r1) break;  // warp-uniform
-      uint32_t gn = 0u, en = 0u;  // 4-bit masks: above / inside the range
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool v = (ok[u] >> e) & 1u;
-        const uint32_t key = kv[u][e];
-        gn |= (v && key > rhi ? 1u : 0u) << e;
-        en |= (v && key >= rlo && key <= rhi ? 1u : 0u) << e;
-      }
-      const int sh4 = 4 * (lane & 7);
-      uint32_t gw = gn << sh4, ew = en << sh4;
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) {
-        gw |= __shfl_xor_sync(0xffffffffu, gw, o);
-        ew |= __shfl_xor_sync(0xffffffffu, ew, o);
-      }
-      const int word = (s0 + u) * 4 + (lane >> 3);
-      if ((lane & 7) == 0 && word < nwu) {
-        gt_out[word] = gw;
-        if (exact) eq_out[word] = ew;
-      }
-      if (!exact && __any_sync(0xffffffffu, en != 0u)) {
-        const uint32_t c = __popc(en);
-        const uint32_t incl = warp_incl_scan(c, lane);
-        uint32_t slot = 0;
-        if (lane == 31) slot = atomicAdd(cand_cnt, incl);
-        slot = __shfl_sync(0xffffffffu, slot, 31) + incl - c;
-        const int p0 = ((s0 + u) * 32 + lane) * 4;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if ((en >> e) & 1u) {
-            if (slot < static_cast<uint32_t>(kRCand))
-              cand_out[slot] = make_uint2(kv[u][e], static_cast<uint32_t>(p0 + e));
-            ++slot;
-          }
-      }
-    }
+    mark_load(R, s0, r1, kv, ok);
+    mark_step(R, kv, ok, s0, r1, rlo, rhi, exact, gt_out, eq_out, cand_cnt, cand_out);
   }
 }
 
@@ -1028,11 +1057,15 @@ __global__ void __launch_bounds__(kSThreads) topk_hist_kernel(const TopkLaunch P
   const int q0 = blockIdx.x * P.seg_quads;
   if (R.n <= P.k || q0 >= R.nq) return;
   const int q1 = min(R.nq, q0 + P.seg_quads);
+  // the first step's keys in flight while the window is sampled
+  uint32_t kv0[kU][4], ok0[kU];
+  hist_load<kSThreads>(R, q0, q1, kv0, ok0);
   for (int i = threadIdx.x; i < kWBins; i += kSThreads) hist[i] = 0u;
   sample_window<kSThreads>(R, misc + 32, misc);  // its barriers also publish the zeroed bins
   const uint32_t wlo = misc[0];
   const int wshift = range_shift(wlo, misc[1], kWBits);
-  const bool nan_seen = window_hist_pass<kSThreads>(R, q0, q1, wlo, wshift, hist);
+  bool nan_seen = hist_step(kv0, ok0, wlo, wshift, hist);
+  nan_seen |= window_hist_pass<kSThreads>(R, q0 + kSThreads * kU, q1, wlo, wshift, hist);
   if (__any_sync(0xffffffffu, nan_seen) && (threadIdx.x & 31) == 0) raise_err(P.d_err, DSA_DEVERR_NAN);
   __syncthreads();
   uint32_t* g = P.ghist + static_cast<long long>(q) * kWBins;
@@ -1051,6 +1084,11 @@ __global__ void __launch_bounds__(kSThreads) topk_mark_kernel(const TopkLaunch P
   const int q0 = blockIdx.x * P.seg_quads;
   if (R.n <= P.k || q0 >= R.nq) return;
   const int q1 = min(R.nq, q0 + P.seg_quads);
+  const int r0 = q0 / 32, r1 = (q1 + 31) / 32;
+  // the first step's keys in flight while the window and the bin are found
+  uint32_t kv0[kU][4], ok0[kU];
+  const int s0 = r0 + (static_cast<int>(threadIdx.x) >> 5) * kU;
+  mark_load(R, s0, r1, kv0, ok0);
   const uint32_t* g = P.ghist + static_cast<long long>(q) * kWBins;
   for (int i = threadIdx.x; i < kWBins; i += kSThreads) hist[i] = __ldcg(g + i);
   sample_window<kSThreads>(R, misc + 32, misc);
@@ -1061,9 +1099,11 @@ __global__ void __launch_bounds__(kSThreads) topk_mark_kernel(const TopkLaunch P
   if (misc[6] > static_cast<uint32_t>(kRCand)) return;  // crowded: K3 resolves the row alone
   uint32_t rlo, rhi;
   window_range(wlo, wshift, misc[4], &rlo, &rhi);
-  mark_pass<kSThreads>(R, q0 / 32, (q1 + 31) / 32, rlo, rhi, false,
-                       P.gbits + static_cast<long long>(q) * P.nw, nullptr, P.gcnt + q,
-                       P.gcand + static_cast<long long>(q) * kRCand);
+  uint32_t* gt_out = P.gbits + static_cast<long long>(q) * P.nw;
+  uint2* cand_out = P.gcand + static_cast<long long>(q) * kRCand;
+  mark_step(R, kv0, ok0, s0, r1, rlo, rhi, false, gt_out, nullptr, P.gcnt + q, cand_out);
+  mark_pass<kSThreads>(R, r0 + (kSThreads / 32) * kU, r1, rlo, rhi, false, gt_out, nullptr,
+                       P.gcnt + q, cand_out);
 }
 
 // ---------------------------------------------------------------- K3
