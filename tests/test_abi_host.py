@@ -157,3 +157,18 @@ def test_selftest_bounded_wait_rejects_bad_limits(lib):
     assert lib.dsa_selftest_bounded_wait(-1, ctypes.c_void_p(16), ctypes.c_void_p(16), None) == C.DSA_ERR_INVALID_ARG
     assert lib.dsa_selftest_bounded_wait(3_000_000, ctypes.c_void_p(16), ctypes.c_void_p(16), None) == C.DSA_ERR_INVALID_ARG
     assert lib.dsa_selftest_bounded_wait(10, None, ctypes.c_void_p(16), None) == C.DSA_ERR_INVALID_ARG
+
+
+def test_shard_merge_host_checks(lib):
+    """The candidate merge's argument checks, before any launch: shard count,
+    k, a negative position bound, the error word; zero rows is a no-op."""
+    p = ctypes.c_void_p(16)
+    args = lambda W, k, bound, err=p: (p, p, p, W, 4, k, bound, p, p, p, p, err, None)  # noqa: E731
+    assert lib.dsa_shard_topk_merge(*args(0, 256, 0)) == C.DSA_ERR_INVALID_ARG
+    assert lib.dsa_shard_topk_merge(*args(C.MAX_SHARDS + 1, 256, 0)) == C.DSA_ERR_INVALID_ARG
+    assert lib.dsa_shard_topk_merge(*args(2, 0, 0)) == C.DSA_ERR_INVALID_ARG
+    assert lib.dsa_shard_topk_merge(*args(2, 5000, 0)) == C.DSA_ERR_INVALID_ARG
+    assert lib.dsa_shard_topk_merge(*args(2, 256, -1)) == C.DSA_ERR_INVALID_ARG
+    assert lib.dsa_shard_topk_merge(*args(2, 256, 0, None)) == C.DSA_ERR_INVALID_ARG
+    # no rows: nothing to launch
+    assert lib.dsa_shard_topk_merge(p, p, p, 2, 0, 256, 1000, p, p, p, p, p, None) == C.DSA_OK
