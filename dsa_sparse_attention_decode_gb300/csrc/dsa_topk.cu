@@ -1074,7 +1074,9 @@ __global__ void __launch_bounds__(kSThreads) topk_hist_kernel(const TopkLaunch P
 }
 
 // ---------------------------------------------------------------- K2
-__global__ void __launch_bounds__(kSThreads) topk_mark_kernel(const TopkLaunch P) {
+// at most 64 registers, so that four CTAs fit on an SM (the pass is latency-
+// bound: at 73 registers three fit, and it ran 2-6 % slower)
+__global__ void __launch_bounds__(kSThreads, 4) topk_mark_kernel(const TopkLaunch P) {
   __shared__ __align__(16) uint32_t hist[kWBins];
   __shared__ uint32_t misc[128];
   const int q = blockIdx.y;
