@@ -47,13 +47,16 @@ def test_config4_reduced_ragged_fp8():
     _run(config_spec(4, B=9, L_lo=300, L_hi=12000))
 
 
-@pytest.mark.parametrize("cfg,kw", [(1, dict(B=3, L=2500)),
-                                    (4, dict(B=4, L_lo=300, L_hi=9000)),
-                                    (2, dict(B=2, L_lo=1500, L_hi=5000))])
-def test_pages_of_128_tokens(cfg, kw):
-    """128-token pages: the indexer's 64-token boxes start inside a page,
-    every gather resolves a slot beyond 64; bf16 and fp8, MTP rows."""
-    _run(config_spec(cfg, page_size=128, **kw))
+@pytest.mark.parametrize("cfg,kw,page", [(1, dict(B=3, L=2500), 128),
+                                         (4, dict(B=4, L_lo=300, L_hi=9000), 128),
+                                         (2, dict(B=2, L_lo=1500, L_hi=5000), 128),
+                                         (1, dict(B=3, L=2500), 192),
+                                         (4, dict(B=3, L_lo=300, L_hi=9000), 192)])
+def test_pages_of_128_and_192_tokens(cfg, kw, page):
+    """Pages of 128 and 192 tokens: the indexer's 64-token boxes start inside
+    a page, gathers resolve slots beyond 64, and 192 takes the division path
+    instead of the shift; bf16 and fp8, MTP rows."""
+    _run(config_spec(cfg, page_size=page, **kw))
 
 
 @pytest.mark.parametrize("rpr,dtype", [(9, "bf16"), (20, "fp8_e4m3"), (33, "bf16")])
