@@ -43,6 +43,13 @@ def test_config3_reduced_sharded(W, L):
     _run(config_spec(3, B=2, L=L, shards=W), sharded=True)
 
 
+@pytest.mark.parametrize("W,L", [(2, 5001), (4, 9001)])
+def test_sharded_fp8_caches(W, L):
+    """The sharded path on fp8 index-K and latent caches: each shard's own
+    scales, and the tensor-core attention over W shard caches at once."""
+    _run(config_spec(3, B=2, L=L, shards=W, dtype="fp8_e4m3"), sharded=True)
+
+
 def test_config4_reduced_ragged_fp8():
     _run(config_spec(4, B=9, L_lo=300, L_hi=12000))
 
